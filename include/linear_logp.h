@@ -1,0 +1,127 @@
+/*
+ * linear_logp.h -- C ABI of the fused linear selected-token log-probability
+ * on GB300 (sm_103a).
+ *
+ * The operation ("Fused Linear LogP", Reference Semantics and Tensor Contract;
+ * per-row temperature from "Feat/nemotron h lm head logprob cuda", summary):
+ *
+ *     z[n, v]  = (hidden[n, :] . weight[v, :] + bias[v]) / temperature[n]
+ *     lse[n]   = log sum_v exp(z[n, v])
+ *     logp[n]  = z[n, targets[n]] - lse[n]
+ *
+ * and its gradients ("add backward support for fused logp CUDA kernels",
+ * Implementation details):
+ *
+ *     dz[n, v]        = grad_logp[n] / temperature[n] * (onehot(targets[n])[v] - exp(z[n, v] - lse[n]))
+ *     grad_hidden     = dz . weight          [N, D]
+ *     grad_weight     = dz^T . hidden        [V, D]
+ *     grad_bias       = sum_n dz[n, :]       [V]
+ *
+ * The [N, V] logits never reach global memory in the forward.  A row whose
+ * target equals ignore_index or lies outside [0, V) is invalid: logp = 0,
+ * lse = -inf, and it contributes nothing to any gradient; its target,
+ * temperature and grad_logp entries are never used in arithmetic
+ * ("recursive deterministic LogP autograd on B200", Summary: invalid token
+ * ids give zero log-probability and -inf log-sum-exp).
+ *
+ * Determinism: every reduction runs in a fixed order that depends only on
+ * (D, V) for per-row results, so logp / lse / grad_hidden rows are bitwise
+ * identical for any batch size N and across runs; grad_weight / grad_bias are
+ * bitwise reproducible across runs for a given input.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers into the current device's
+ *     memory, row-major and contiguous.  bf16 tensors are passed as raw
+ *     16-bit storage (void*).  The caller owns every buffer; the library
+ *     allocates nothing and keeps no per-call state.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued on it; the library never synchronises.
+ *   - Alignment: hidden, weight, grad_hidden, grad_weight and workspace must be
+ *     16-byte aligned; bias 16-byte aligned; float arrays 4-byte aligned;
+ *     targets 8-byte aligned.
+ *   - Shapes: N >= 0, 1 <= D, D % 8 == 0 (16-byte rows for the tensor-memory
+ *     copies), 1 <= V, and N, D, V < 2^31 with N*D, V*D and N*V < 2^62.
+ *   - N == 0: the forward is a no-op and the backward writes zeros into
+ *     grad_weight / grad_bias (sums over no tokens); per-token pointers may
+ *     then be NULL.  Both return LLP_OK.
+ *   - Invalid arguments are reported BEFORE anything is enqueued; the outputs
+ *     are then untouched.  There is no fallback path.
+ *   - temperature values must be finite and > 0 (not checked on the device).
+ */
+#ifndef LINEAR_LOGP_H_
+#define LINEAR_LOGP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  LLP_OK = 0,
+  LLP_ERR_NULL_POINTER = -1,        /* a required pointer is NULL */
+  LLP_ERR_BAD_SHAPE = -2,           /* N < 0, D < 1, V < 1, D % 8 != 0, or too large */
+  LLP_ERR_MISALIGNED = -3,          /* a pointer violates the alignment rules above */
+  LLP_ERR_UNSUPPORTED_DEVICE = -4,  /* the current device is not an sm_103 GPU */
+  LLP_ERR_WORKSPACE_TOO_SMALL = -5, /* workspace_bytes below the *_workspace_bytes() query */
+  LLP_ERR_CUDA = -6,                /* a CUDA runtime / driver call or launch failed */
+  LLP_ERR_DEVICE_TIMEOUT = -7       /* a kernel gave up on a wait (see linear_logp_device_status) */
+};
+
+/* Bytes of workspace linear_logp_fwd needs for an N x D x V problem
+ * (0 when N == 0).  The workspace holds the per-vocab-split (max, sum) pairs
+ * and the captured target logits. */
+size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V);
+
+/* Bytes of workspace linear_logp_bwd needs: the bf16 dlogits buffer
+ * [N, round_up(V, 64)], the grad_bias partials when has_bias != 0, and the fp32
+ * K-segment partials of grad_hidden (V > 32768) and grad_weight (N > 32768). */
+size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_bias);
+
+/*
+ * Forward.
+ *   hidden       [N, D] bf16            (required)
+ *   weight       [V, D] bf16            (required)
+ *   bias         [V] fp32 or NULL
+ *   targets      [N] int64              (required)
+ *   temperature  [N] fp32 or NULL (NULL = 1)
+ *   ignore_index   target value that marks an ignored row (e.g. -100)
+ *   out_logp     [N] fp32  (required; overwritten)
+ *   out_lse      [N] fp32  (required; overwritten; the backward needs it)
+ *   workspace    device scratch of at least linear_logp_fwd_workspace_bytes()
+ * Returns LLP_OK or a negative LLP_ERR_* code.
+ */
+int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                    const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                    float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward.  Same inputs as the forward plus
+ *   grad_logp    [N] fp32  upstream gradient of logp (required)
+ *   saved_lse    [N] fp32  out_lse of the forward on the same inputs (required)
+ * Outputs (each may be NULL to skip it; all NULL is a no-op):
+ *   grad_hidden  [N, D] bf16  (overwritten, not accumulated)
+ *   grad_weight  [V, D] bf16  (overwritten)
+ *   grad_bias    [V] fp32     (overwritten; requires bias != NULL)
+ *   workspace    device scratch of at least linear_logp_bwd_workspace_bytes()
+ */
+int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                    const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                    int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* linear_logp_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the current device's kernel
+ * status word.  Returns LLP_OK if no kernel gave up on a wait since the last
+ * call, LLP_ERR_DEVICE_TIMEOUT if one did (the detailed code goes to
+ * *device_code when it is not NULL), or LLP_ERR_CUDA. */
+int linear_logp_device_status(void* stream, unsigned int* device_code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINEAR_LOGP_H_ */

@@ -1,0 +1,87 @@
+"""ctypes loader for ``liblinear_logp.so`` (the C ABI in include/linear_logp.h).
+
+Argument marshalling only.  If the library is missing or fails to load, every
+call raises: there is no fallback implementation anywhere in this package.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+LLP_OK = 0
+LLP_ERR_NULL_POINTER = -1
+LLP_ERR_BAD_SHAPE = -2
+LLP_ERR_MISALIGNED = -3
+LLP_ERR_UNSUPPORTED_DEVICE = -4
+LLP_ERR_WORKSPACE_TOO_SMALL = -5
+LLP_ERR_CUDA = -6
+LLP_ERR_DEVICE_TIMEOUT = -7
+
+EXPORTED = (
+    "linear_logp_fwd_workspace_bytes",
+    "linear_logp_bwd_workspace_bytes",
+    "linear_logp_fwd",
+    "linear_logp_bwd",
+    "linear_logp_status_string",
+    "linear_logp_device_status",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_size = ctypes.c_size_t
+
+
+class LinearLogpError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                "(or lm_head_selected_gb300.build.build()); there is no fallback path")
+        lib = ctypes.CDLL(path)
+        lib.linear_logp_fwd_workspace_bytes.argtypes = [_i64, _i64, _i64]
+        lib.linear_logp_fwd_workspace_bytes.restype = _size
+        lib.linear_logp_bwd_workspace_bytes.argtypes = [_i64, _i64, _i64, ctypes.c_int]
+        lib.linear_logp_bwd_workspace_bytes.restype = _size
+        lib.linear_logp_fwd.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _p, _p, _size, _p]
+        lib.linear_logp_fwd.restype = ctypes.c_int
+        lib.linear_logp_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _p, _p, _p,
+                                        _size, _p]
+        lib.linear_logp_bwd.restype = ctypes.c_int
+        lib.linear_logp_status_string.argtypes = [ctypes.c_int]
+        lib.linear_logp_status_string.restype = ctypes.c_char_p
+        lib.linear_logp_device_status.argtypes = [_p, ctypes.POINTER(ctypes.c_uint)]
+        lib.linear_logp_device_status.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().linear_logp_status_string(int(status)).decode()
+
+
+def check(fn: str, status: int) -> None:
+    if status != LLP_OK:
+        raise LinearLogpError(fn, status, status_string(status))

@@ -1,0 +1,390 @@
+// C ABI of the fused linear selected-token log-probability: argument checks,
+// workspace layout, tensor-memory-copy descriptors and the launch sequence.
+// Declarations and the contract are in include/linear_logp.h.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "linear_logp.h"
+#include "llp_internal.h"
+
+namespace {
+
+// Kernel status word: a kernel that gives up on a bounded wait records why here.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInit {
+  bool done = false;
+  int status = LLP_OK;
+  int num_sms = 0;
+  unsigned int* status_ptr = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInit g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int load_encode_fn() {
+  static std::once_flag once;
+  static int st = LLP_OK;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      st = LLP_ERR_CUDA;
+    } else {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  return st;
+}
+
+// Per-device one-time set-up with that device current: architecture check,
+// shared-memory opt-in for every kernel, SM count, status-word address.
+int init_device(DeviceInit** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LLP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LLP_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInit& d = g_dev[dev];
+  if (!d.done) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return LLP_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) {
+      d.status = LLP_ERR_UNSUPPORTED_DEVICE;
+    } else if (llp::fwd_setup() != cudaSuccess || llp::bwd_setup() != cudaSuccess ||
+               cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_ptr), g_status_word) != cudaSuccess) {
+      d.status = LLP_ERR_CUDA;
+    } else {
+      d.status = LLP_OK;
+    }
+    d.num_sms = sms;
+    d.done = true;
+  }
+  *out = &d;
+  return d.status;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+constexpr int64_t kLim31 = (int64_t(1) << 31) - 1;
+constexpr int64_t kLim62 = int64_t(1) << 62;
+
+bool product_ok(int64_t a, int64_t b) { return a == 0 || b <= kLim62 / a; }
+
+int check_shapes(int64_t N, int64_t D, int64_t V) {
+  if (N < 0 || D < 1 || V < 1 || (D % 8) != 0) return LLP_ERR_BAD_SHAPE;
+  if (N > kLim31 || D > kLim31 || V > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (!product_ok(N, D) || !product_ok(V, D) || !product_ok(N, round_up(V, 64))) return LLP_ERR_BAD_SHAPE;
+  // every work-unit count and tile index must fit a 32-bit int
+  const int64_t num_m = cdiv(N, llp::kTileM);
+  const int64_t num_vt = cdiv(V, llp::kTileN);
+  const int64_t num_d = cdiv(D, llp::kTileN);
+  if (num_m * num_vt > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (cdiv(V, llp::kKSegment) * num_m * num_d > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (cdiv(N, llp::kKSegment) * cdiv(V, llp::kTileM) * num_d > kLim31) return LLP_ERR_BAD_SHAPE;
+  return LLP_OK;
+}
+
+int check_inputs(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                 const float* temperature, int64_t N, int64_t D, int64_t V) {
+  if (hidden == nullptr || weight == nullptr || targets == nullptr) return LLP_ERR_NULL_POINTER;
+  const int s = check_shapes(N, D, V);
+  if (s != LLP_OK) return s;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8)) return LLP_ERR_MISALIGNED;
+  if (bias != nullptr && !aligned(bias, 16)) return LLP_ERR_MISALIGNED;
+  if (temperature != nullptr && !aligned(temperature, 4)) return LLP_ERR_MISALIGNED;
+  return LLP_OK;
+}
+
+// Workspace carving: each region starts on a 256-byte boundary from the base.
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  }
+};
+
+struct FwdLayout {
+  size_t part_m, part_s, zt, total;
+};
+
+FwdLayout fwd_layout(int64_t N, int64_t V) {
+  const size_t S = static_cast<size_t>(cdiv(V, llp::kSplitWidth));
+  Carver c;
+  FwdLayout L;
+  L.part_m = c.take(S * N * sizeof(float));
+  L.part_s = c.take(S * N * sizeof(float));
+  L.zt = c.take(N * sizeof(float));
+  L.total = c.off;
+  return L;
+}
+
+struct BwdLayout {
+  size_t dz, gb_part, dh_part, dw_part, total;
+  bool has_gb, has_dh, has_dw;
+};
+
+BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, bool want_dw) {
+  const size_t V_pad = round_up(static_cast<size_t>(V), 64);
+  const size_t num_m = static_cast<size_t>(cdiv(N, llp::kTileM));
+  const size_t nseg_v = static_cast<size_t>(cdiv(V, llp::kKSegment));
+  const size_t nseg_n = static_cast<size_t>(cdiv(N, llp::kKSegment));
+  Carver c;
+  BwdLayout L;
+  L.dz = c.take(static_cast<size_t>(N) * V_pad * 2);
+  L.has_gb = bias;
+  L.gb_part = bias ? c.take(num_m * 4 * static_cast<size_t>(V) * sizeof(float)) : 0;
+  L.has_dh = want_dh && nseg_v > 1;
+  L.dh_part = L.has_dh ? c.take(nseg_v * static_cast<size_t>(N) * D * sizeof(float)) : 0;
+  L.has_dw = want_dw && nseg_n > 1;
+  L.dw_part = L.has_dw ? c.take(nseg_n * static_cast<size_t>(V) * D * sizeof(float)) : 0;
+  L.total = c.off;
+  return L;
+}
+
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+             uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
+}
+
+int grid_for(int64_t units, int num_sms) {
+  return static_cast<int>(units < num_sms ? units : num_sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V) {
+  if (N <= 0 || check_shapes(N, D, V) != LLP_OK) return 0;
+  return fwd_layout(N, V).total;
+}
+
+size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_bias) {
+  if (N <= 0 || check_shapes(N, D, V) != LLP_OK) return 0;
+  return bwd_layout(N, D, V, has_bias != 0, true, true).total;
+}
+
+const char* linear_logp_status_string(int status) {
+  switch (status) {
+    case LLP_OK: return "ok";
+    case LLP_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case LLP_ERR_BAD_SHAPE: return "unsupported shape (need N >= 0, D >= 1, V >= 1, D % 8 == 0, sizes in range)";
+    case LLP_ERR_MISALIGNED: return "misaligned pointer";
+    case LLP_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+    case LLP_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case LLP_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case LLP_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                    const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                    float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shapes(N, D, V);
+  if (st != LLP_OK) return st;
+  if (N == 0) return LLP_OK;  // nothing to compute; per-token pointers may be NULL
+  st = check_inputs(hidden, weight, bias, targets, temperature, N, D, V);
+  if (st != LLP_OK) return st;
+  if (out_logp == nullptr || out_lse == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(out_logp, 4) || !aligned(out_lse, 4)) return LLP_ERR_MISALIGNED;
+  const FwdLayout L = fwd_layout(N, V);
+  if (workspace == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
+  if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap tm_h, tm_w;
+  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kTileN) != LLP_OK) return LLP_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  llp::FwdParams p;
+  p.N = static_cast<int>(N);
+  p.D = static_cast<int>(D);
+  p.V = static_cast<int>(V);
+  p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+  p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
+  p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
+  p.group_m = llp::kGroupM;
+  p.bias = bias;
+  p.targets = reinterpret_cast<const long long*>(targets);
+  p.temperature = temperature;
+  p.ignore_index = ignore_index;
+  p.part_m = reinterpret_cast<float*>(ws + L.part_m);
+  p.part_s = reinterpret_cast<float*>(ws + L.part_s);
+  p.zt = reinterpret_cast<float*>(ws + L.zt);
+  p.err = dev->status_ptr;
+
+  const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+  return LLP_OK;
+}
+
+int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                    const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                    int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shapes(N, D, V);
+  if (st != LLP_OK) return st;
+  if (grad_bias != nullptr && bias == nullptr) return LLP_ERR_NULL_POINTER;
+  if ((grad_hidden && !aligned(grad_hidden, 16)) || (grad_weight && !aligned(grad_weight, 16)) ||
+      (grad_bias && !aligned(grad_bias, 4)))
+    return LLP_ERR_MISALIGNED;
+  if (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr) return LLP_OK;
+
+  DeviceInit* dev = nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    // Sums over an empty set of tokens: the weight and bias gradients are zero.
+    // The per-token pointers (hidden, targets, grad_logp, saved_lse) may be NULL.
+    if ((st = init_device(&dev)) != LLP_OK) return st;
+    if (grad_weight && cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * D * 2, s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    if (grad_bias && cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(V) * sizeof(float), s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    return LLP_OK;
+  }
+  st = check_inputs(hidden, weight, bias, targets, temperature, N, D, V);
+  if (st != LLP_OK) return st;
+  if (grad_logp == nullptr || saved_lse == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(grad_logp, 4) || !aligned(saved_lse, 4)) return LLP_ERR_MISALIGNED;
+  const bool want_gb = grad_bias != nullptr;
+  const BwdLayout L = bwd_layout(N, D, V, bias != nullptr, grad_hidden != nullptr, grad_weight != nullptr);
+  if (workspace == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
+  if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t V_pad = static_cast<int64_t>(round_up(static_cast<size_t>(V), 64));
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + L.dz);
+
+  // B1: dlogits (+ grad_bias partials)
+  {
+    CUtensorMap tm_h, tm_w;
+    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kTileN) != LLP_OK) return LLP_ERR_CUDA;
+    llp::DzParams p;
+    p.N = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.V = static_cast<int>(V);
+    p.V_pad = static_cast<int>(V_pad);
+    p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+    p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
+    p.group_m = llp::kGroupM;
+    p.bias = bias;
+    p.targets = reinterpret_cast<const long long*>(targets);
+    p.temperature = temperature;
+    p.ignore_index = ignore_index;
+    p.grad_logp = grad_logp;
+    p.lse = saved_lse;
+    p.dz = dz;
+    p.gb_part = want_gb ? reinterpret_cast<float*>(ws + L.gb_part) : nullptr;
+    p.err = dev->status_ptr;
+    const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
+    if (llp::launch_dlogits(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+  }
+
+  // B2: grad_hidden = dz . W over fixed vocab segments
+  if (grad_hidden != nullptr) {
+    CUtensorMap tm_dz, tm_w_mn;
+    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    llp::GradGemmParams p;
+    p.rows = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.K = static_cast<int>(V);
+    p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
+    p.nseg = static_cast<int>(cdiv(V, llp::kKSegment));
+    p.kseg_blocks = llp::kKSegment / llp::kTileK;
+    p.out = static_cast<__nv_bfloat16*>(grad_hidden);
+    p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
+    p.err = dev->status_ptr;
+    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
+    if (llp::launch_grad_hidden(tm_dz, tm_w_mn, p, grid_for(units, dev->num_sms), s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    if (p.nseg > 1 &&
+        llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+  }
+
+  // B3: grad_weight = dz^T . h over fixed token segments
+  if (grad_weight != nullptr) {
+    CUtensorMap tm_dz_mn, tm_h_mn;
+    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    llp::GradGemmParams p;
+    p.rows = static_cast<int>(V);
+    p.D = static_cast<int>(D);
+    p.K = static_cast<int>(N);
+    p.num_m = static_cast<int>(cdiv(V, llp::kTileM));
+    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
+    p.nseg = static_cast<int>(cdiv(N, llp::kKSegment));
+    p.kseg_blocks = llp::kKSegment / llp::kTileK;
+    p.out = static_cast<__nv_bfloat16*>(grad_weight);
+    p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
+    p.err = dev->status_ptr;
+    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
+    if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, p, grid_for(units, dev->num_sms), s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    if (p.nseg > 1 &&
+        llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+  }
+
+  // B4: grad_bias
+  if (want_gb) {
+    const int nblocks = static_cast<int>(cdiv(N, llp::kTileM) * 4);
+    if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
+                             s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+  }
+  return LLP_OK;
+}
+
+int linear_logp_device_status(void* stream, unsigned int* device_code) {
+  DeviceInit* dev = nullptr;
+  const int st = init_device(&dev);
+  if (st != LLP_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLP_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return LLP_ERR_CUDA;
+  if (device_code != nullptr) *device_code = v;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return LLP_ERR_CUDA;
+    return LLP_ERR_DEVICE_TIMEOUT;
+  }
+  return LLP_OK;
+}
+
+}  // extern "C"

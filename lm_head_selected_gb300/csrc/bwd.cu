@@ -1,0 +1,335 @@
+// Backward of the fused linear selected-token log-probability on tcgen05.
+//
+//   B1  dlogits: recompute each 128 x 256 logit tile exactly as the forward
+//       does, then  dz = (g_n / tau_n) * (onehot(t_n) - exp(z - lse_n)),
+//       selected to 0 on invalid rows (so a NaN upstream gradient there cannot
+//       leak), written as bf16 into a [N, V_pad] workspace.  With a bias, each
+//       warp also reduces its 32 rows of dz per column in a fixed butterfly
+//       order into a [N/32, V] fp32 partial for grad_bias.
+//   B2  grad_hidden = dz . W        (M = tokens, N = hidden, K = vocab)
+//   B3  grad_weight = dz^T . h      (M = vocab,  N = hidden, K = tokens)
+//       Both are tcgen05 GEMMs over fixed K segments of kKSegment; with more
+//       than one segment the fp32 segment partials are summed in ascending
+//       order and rounded once to bf16.
+//   B4  grad_bias[v] = sum of the 32-row partials in ascending row order.
+//
+// The formula is the one of "add backward support for fused logp CUDA
+// kernels" (Implementation details: grad_out * (one_hot - softmax) from saved
+// softmax statistics, no logits-sized probability tensor); the 1/tau factor
+// is the chain rule through the temperature of "Feat/nemotron h lm head
+// logprob cuda".  The fixed ascending K segments with fp32 partials follow
+// the same page's fix for reductions longer than 32768 ("split into <= 32768
+// segments whose FP32 partials are summed in a fixed ascending order"); here
+// fp32 accumulation in TMEM has no length limit, the segments only fix the
+// reduction order and spread the long vocab reduction over more SMs.
+#include "gemm_core.cuh"
+
+namespace llp {
+
+constexpr float kLog2eB = 1.4426950408889634f;
+
+__device__ __forceinline__ bool target_ok(long long t, int V, long long ignore_index) {
+  return t != ignore_index && t >= 0 && t < static_cast<long long>(V);
+}
+
+// Column sums of a 32 x 32 block held one row per lane: on return lane l holds
+// the sum over the 32 lanes of column l.  Butterfly order, fixed.
+__device__ __forceinline__ float warp_column_sums(float (&x)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? x[i] : x[i + off];
+      const float keep = upper ? x[i + off] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return x[0];
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ----------------------------------------------------------------------------
+// B1: dlogits
+// ----------------------------------------------------------------------------
+template <bool HAS_BIAS>
+struct DzCfg {
+  static constexpr bool A_MN = false;
+  static constexpr bool B_MN = false;
+  static constexpr int BN = kTileN;
+  static constexpr int STAGES = 4;
+  static constexpr int EXTRA_SMEM = 0;
+  using Params = DzParams;
+
+  struct RowState {
+    float inv_tau, gs, lse;
+    int t;
+    int n;
+    bool valid;
+  };
+
+  static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_last(); }
+  static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+
+  static __device__ __forceinline__ int num_units(const Params& p) { return p.num_m * p.num_vt; }
+
+  static __device__ __forceinline__ UnitInfo unit(const Params& p, int u) {
+    const int gsize = p.group_m * p.num_vt;
+    const int grp = u / gsize;
+    const int r = u - grp * gsize;
+    const int gm = min(p.group_m, p.num_m - grp * p.group_m);
+    const int vt = r / gm;
+    const int mt = grp * p.group_m + (r - vt * gm);
+    UnitInfo ui;
+    ui.m0 = mt * BM;
+    ui.n0 = vt * BN;
+    ui.ntiles = 1;
+    ui.kb0 = 0;
+    ui.nkb = (p.D + BK - 1) / BK;
+    return ui;
+  }
+
+  static __device__ __forceinline__ void unit_begin(const Params& p, const UnitInfo& ui, int, int row, RowState& rs) {
+    rs.n = ui.m0 + row;
+    rs.valid = false;
+    rs.inv_tau = 1.f;
+    rs.gs = 0.f;
+    rs.lse = 0.f;
+    rs.t = -1;
+    if (rs.n < p.N) {
+      const long long t = p.targets[rs.n];
+      if (target_ok(t, p.V, p.ignore_index)) {
+        rs.valid = true;
+        rs.t = static_cast<int>(t);
+        if (p.temperature != nullptr) rs.inv_tau = __frcp_rn(p.temperature[rs.n]);
+        rs.gs = p.grad_logp[rs.n] * rs.inv_tau;
+        rs.lse = p.lse[rs.n];
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int, int, int g, int lane,
+                                              uint32_t taddr, RowState& rs) {
+    const int v0 = ui.n0;
+    const bool full = (v0 + BN) <= p.V;
+    const int mt = ui.m0 / BM;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float z[32];
+      tmem_load_32cols(taddr + c * 32, z);
+      const int vc = v0 + c * 32;
+      if (HAS_BIAS) {
+        if (full) {
+          const float4* b4 = reinterpret_cast<const float4*>(p.bias + vc);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 b = __ldg(b4 + q);
+            z[4 * q + 0] += b.x;
+            z[4 * q + 1] += b.y;
+            z[4 * q + 2] += b.z;
+            z[4 * q + 3] += b.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] += (vc + i < p.V) ? __ldg(p.bias + vc + i) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float zz = z[i] * rs.inv_tau;
+        const float pr = exp2f((zz - rs.lse) * kLog2eB);
+        const float oh = (vc + i == rs.t) ? 1.f : 0.f;
+        float d = rs.gs * (oh - pr);
+        if (!rs.valid || (!full && vc + i >= p.V)) d = 0.f;
+        z[i] = d;
+      }
+      if (rs.n < p.N && vc < p.V_pad) {
+        uint4* dst = reinterpret_cast<uint4*>(p.dz + static_cast<size_t>(rs.n) * p.V_pad + vc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(z[8 * q + 0], z[8 * q + 1]);
+          w.y = pack_bf16x2(z[8 * q + 2], z[8 * q + 3]);
+          w.z = pack_bf16x2(z[8 * q + 4], z[8 * q + 5]);
+          w.w = pack_bf16x2(z[8 * q + 6], z[8 * q + 7]);
+          dst[q] = w;
+        }
+      }
+      if (HAS_BIAS && p.gb_part != nullptr) {  // warp-uniform
+        const float colsum = warp_column_sums(z, lane);
+        const int v = vc + lane;
+        if (v < p.V) p.gb_part[static_cast<size_t>(mt * 4 + g) * p.V + v] = colsum;
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void unit_end(const Params&, const UnitInfo&, int, int, RowState&) {}
+};
+
+// ----------------------------------------------------------------------------
+// B2 / B3: gradient GEMMs with fixed K segments.
+// ----------------------------------------------------------------------------
+template <bool A_MN_, bool B_MN_>
+struct GradCfg {
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
+  static constexpr int BN = kTileN;
+  static constexpr int STAGES = 4;
+  static constexpr int EXTRA_SMEM = 0;
+  using Params = GradGemmParams;
+
+  struct RowState {
+    int r;
+  };
+
+  static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_normal(); }
+  static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+
+  static __device__ __forceinline__ int num_units(const Params& p) { return p.nseg * p.num_m * p.num_d; }
+
+  // Segment is the slowest index, then M tile, then the output column tile, so the
+  // CTAs that run together share A rows and the same K window of B.
+  static __device__ __forceinline__ UnitInfo unit(const Params& p, int u) {
+    const int per_seg = p.num_m * p.num_d;
+    const int seg = u / per_seg;
+    const int r = u - seg * per_seg;
+    const int mt = r / p.num_d;
+    const int dt = r - mt * p.num_d;
+    const int total_kb = (p.K + BK - 1) / BK;
+    UnitInfo ui;
+    ui.m0 = mt * BM;
+    ui.n0 = dt * BN;
+    ui.ntiles = 1;
+    ui.kb0 = seg * p.kseg_blocks;
+    ui.nkb = min(p.kseg_blocks, total_kb - ui.kb0);
+    return ui;
+  }
+
+  static __device__ __forceinline__ void unit_begin(const Params&, const UnitInfo& ui, int, int row, RowState& rs) {
+    rs.r = ui.m0 + row;
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int u, int, int, int, int,
+                                              uint32_t taddr, RowState& rs) {
+    const int seg = u / (p.num_m * p.num_d);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int d0 = ui.n0 + c * 32;
+      if (d0 >= p.D) break;  // warp-uniform
+      float a[32];
+      tmem_load_32cols(taddr + c * 32, a);
+      if (rs.r >= p.rows) continue;
+      if (p.nseg == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rs.r) * p.D + d0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (d0 + 8 * q < p.D) {
+            uint4 w;
+            w.x = pack_bf16x2(a[8 * q + 0], a[8 * q + 1]);
+            w.y = pack_bf16x2(a[8 * q + 2], a[8 * q + 3]);
+            w.z = pack_bf16x2(a[8 * q + 4], a[8 * q + 5]);
+            w.w = pack_bf16x2(a[8 * q + 6], a[8 * q + 7]);
+            dst[q] = w;
+          }
+        }
+      } else {
+        float4* dst =
+            reinterpret_cast<float4*>(p.part + (static_cast<size_t>(seg) * p.rows + rs.r) * p.D + d0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (d0 + 4 * q < p.D) dst[q] = make_float4(a[4 * q + 0], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+        }
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void unit_end(const Params&, const UnitInfo&, int, int, RowState&) {}
+};
+
+// out[i] = bf16( sum_{s ascending} part[s][i] ), 4 elements per thread step.
+__global__ void __launch_bounds__(256) segment_sum_kernel(const float* __restrict__ part, int nseg, long long count,
+                                                          __nv_bfloat16* __restrict__ out) {
+  const long long n4 = count / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(part)[i];
+    for (int s = 1; s < nseg; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(part + static_cast<size_t>(s) * count)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    uint2 w;
+    w.x = pack_bf16x2(acc.x, acc.y);
+    w.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2*>(out)[i] = w;
+  }
+}
+
+// grad_bias[v] = sum over 32-row blocks in ascending order.
+__global__ void __launch_bounds__(256) bias_sum_kernel(const float* __restrict__ gb_part, int nblocks, int V,
+                                                       float* __restrict__ out) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= V) return;
+  float acc = 0.f;
+  for (int b = 0; b < nblocks; ++b) acc += gb_part[static_cast<size_t>(b) * V + v];
+  out[v] = acc;
+}
+
+template <class Cfg>
+static cudaError_t set_smem(void) {
+  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
+  return cudaFuncSetAttribute(tc_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan::TOTAL);
+}
+
+template <class Cfg>
+static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p, int grid,
+                              cudaStream_t s) {
+  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
+  tc_gemm_kernel<Cfg><<<grid, kNumThreads, Plan::TOTAL, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+cudaError_t bwd_setup() {
+  cudaError_t e;
+  if ((e = set_smem<DzCfg<false>>()) != cudaSuccess) return e;
+  if ((e = set_smem<DzCfg<true>>()) != cudaSuccess) return e;
+  if ((e = set_smem<GradCfg<false, true>>()) != cudaSuccess) return e;
+  return set_smem<GradCfg<true, true>>();
+}
+
+cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, int grid,
+                           cudaStream_t s) {
+  return p.bias ? launch_cfg<DzCfg<true>>(tm_h, tm_w, p, grid, s) : launch_cfg<DzCfg<false>>(tm_h, tm_w, p, grid, s);
+}
+
+cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const GradGemmParams& p,
+                               int grid, cudaStream_t s) {
+  return launch_cfg<GradCfg<false, true>>(tm_dz, tm_w_mn, p, grid, s);
+}
+
+cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const GradGemmParams& p,
+                               int grid, cudaStream_t s) {
+  return launch_cfg<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, p, grid, s);
+}
+
+cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s) {
+  const int threads = 256;
+  long long blocks = (count / 4 + threads - 1) / threads;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  segment_sum_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s) {
+  const int threads = 256;
+  bias_sum_kernel<<<(V + threads - 1) / threads, threads, 0, s>>>(gb_part, nblocks, V, out);
+  return cudaGetLastError();
+}
+
+}  // namespace llp

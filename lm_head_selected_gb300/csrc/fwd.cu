@@ -1,0 +1,205 @@
+// Forward of the fused linear selected-token log-probability on tcgen05.
+//
+//   F1  per (128-token tile, 512-column vocab split):
+//         acc = h_tile . W_tile^T on the tensor cores (bf16 in, fp32 in TMEM),
+//         z = (acc + b[v]) * (1/tau_n), folded into a per-row online max/sum,
+//         with z[t_n] captured as the tile holding t_n passes.  Only the
+//         per-split (max, sum) pair and the target logit leave the SM; the
+//         [N, V] logits never reach global memory.
+//   F2  per row: merge the splits in ascending order,
+//         M = max_s m_s,  S = sum_s s_s * exp(m_s - M),
+//         lse = M + log S,  logp = (z_t - M) - log S.
+//
+// Semantics follow "Fused Linear LogP" (Reference Semantics, Tensor Contract):
+// logp = z[target] - logsumexp(z); the per-row temperature of "Feat/nemotron h
+// lm head logprob cuda" divides the biased logit; invalid targets (ignore index
+// or outside [0, V)) give logp = 0 and lse = -inf ("recursive deterministic
+// LogP autograd on B200", Summary), without any read at the target index.
+// The final expression keeps target - max - log(sum) apart, as the
+// deterministic forward in "recursive deterministic LogP autograd on B200"
+// (Prior art table) does.
+#include "gemm_core.cuh"
+
+namespace llp {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ bool target_valid(long long t, int V, long long ignore_index) {
+  return t != ignore_index && t >= 0 && t < static_cast<long long>(V);
+}
+
+template <bool HAS_BIAS>
+struct FwdCfg {
+  static constexpr bool A_MN = false;
+  static constexpr bool B_MN = false;
+  static constexpr int BN = kTileN;
+  static constexpr int STAGES = 4;
+  static constexpr int EXTRA_SMEM = 0;
+  static constexpr int TPS = kTilesPerSplit;
+  using Params = FwdParams;
+
+  struct RowState {
+    float m;        // running max over the split
+    float s;        // running sum of exp(z - m)
+    float zt;       // captured target logit
+    float inv_tau;  // 1 / tau for this row
+    int tloc;       // target column relative to the unit's first column (may be out of range)
+    int n;          // token row
+  };
+
+  static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_last(); }
+  static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+
+  static __device__ __forceinline__ int num_units(const Params& p) { return p.num_m * p.num_splits; }
+
+  // Raster: groups of group_m token tiles; inside a group the vocab split is the
+  // slow index, so concurrently running CTAs share the same weight tiles in L2.
+  static __device__ __forceinline__ UnitInfo unit(const Params& p, int u) {
+    const int gsize = p.group_m * p.num_splits;
+    const int grp = u / gsize;
+    const int r = u - grp * gsize;
+    const int gm = min(p.group_m, p.num_m - grp * p.group_m);
+    const int split = r / gm;
+    const int mt = grp * p.group_m + (r - split * gm);
+    UnitInfo ui;
+    ui.m0 = mt * BM;
+    ui.n0 = split * TPS * BN;
+    ui.ntiles = min(TPS, p.num_vt - split * TPS);
+    ui.kb0 = 0;
+    ui.nkb = (p.D + BK - 1) / BK;
+    return ui;
+  }
+
+  static __device__ __forceinline__ void unit_begin(const Params& p, const UnitInfo& ui, int, int row, RowState& rs) {
+    rs.n = ui.m0 + row;
+    rs.m = -INFINITY;
+    rs.s = 0.f;
+    rs.zt = 0.f;
+    rs.inv_tau = 1.f;
+    rs.tloc = -1;
+    if (rs.n < p.N) {
+      const long long t = p.targets[rs.n];
+      if (target_valid(t, p.V, p.ignore_index)) rs.tloc = static_cast<int>(t - ui.n0);
+      if (p.temperature != nullptr) rs.inv_tau = __frcp_rn(p.temperature[rs.n]);
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int j, int, int, int,
+                                              uint32_t taddr, RowState& rs) {
+    const int v0 = ui.n0 + j * BN;
+    const bool full = (v0 + BN) <= p.V;
+    const int tl = rs.tloc - j * BN;
+    const bool mine = (tl >= 0) && (tl < BN);
+    const bool any_t = __any_sync(0xffffffffu, mine);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float z[32];
+      tmem_load_32cols(taddr + c * 32, z);
+      const int vc = v0 + c * 32;
+      if (HAS_BIAS) {
+        if (full) {
+          const float4* b4 = reinterpret_cast<const float4*>(p.bias + vc);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 b = __ldg(b4 + q);
+            z[4 * q + 0] += b.x;
+            z[4 * q + 1] += b.y;
+            z[4 * q + 2] += b.z;
+            z[4 * q + 3] += b.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] += (vc + i < p.V) ? __ldg(p.bias + vc + i) : 0.f;
+        }
+      }
+      float cm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        z[i] *= rs.inv_tau;
+        if (!full && vc + i >= p.V) z[i] = -INFINITY;
+        cm = fmaxf(cm, z[i]);
+      }
+      if (any_t) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (tl == c * 32 + i) rs.zt = z[i];
+      }
+      const float mn = fmaxf(rs.m, cm);
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        a0 += exp2f((z[i + 0] - mn) * kLog2e);
+        a1 += exp2f((z[i + 1] - mn) * kLog2e);
+        a2 += exp2f((z[i + 2] - mn) * kLog2e);
+        a3 += exp2f((z[i + 3] - mn) * kLog2e);
+      }
+      rs.s = rs.s * exp2f((rs.m - mn) * kLog2e) + ((a0 + a1) + (a2 + a3));
+      rs.m = mn;
+    }
+  }
+
+  static __device__ __forceinline__ void unit_end(const Params& p, const UnitInfo& ui, int, int, RowState& rs) {
+    if (rs.n >= p.N) return;
+    const int split = ui.n0 / (TPS * BN);
+    const size_t idx = static_cast<size_t>(split) * p.N + rs.n;
+    p.part_m[idx] = rs.m;
+    p.part_s[idx] = rs.s;
+    if (rs.tloc >= 0 && rs.tloc < ui.ntiles * BN) p.zt[rs.n] = rs.zt;
+  }
+};
+
+__global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __restrict__ out_logp,
+                                                        float* __restrict__ out_lse) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= p.N) return;
+  const long long t = p.targets[n];
+  if (!target_valid(t, p.V, p.ignore_index)) {
+    out_logp[n] = 0.f;
+    out_lse[n] = -INFINITY;
+    return;
+  }
+  float M = -INFINITY;
+  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, p.part_m[static_cast<size_t>(s) * p.N + n]);
+  float S = 0.f;
+  for (int s = 0; s < p.num_splits; ++s) {
+    const size_t i = static_cast<size_t>(s) * p.N + n;
+    S += p.part_s[i] * exp2f((p.part_m[i] - M) * kLog2e);
+  }
+  const float ls = logf(S);
+  out_lse[n] = M + ls;
+  out_logp[n] = (p.zt[n] - M) - ls;
+}
+
+template <class Cfg>
+static cudaError_t set_smem(void) {
+  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
+  return cudaFuncSetAttribute(tc_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan::TOTAL);
+}
+
+cudaError_t fwd_setup() {
+  cudaError_t e = set_smem<FwdCfg<false>>();
+  if (e != cudaSuccess) return e;
+  return set_smem<FwdCfg<true>>();
+}
+
+template <class Cfg>
+static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p, int grid,
+                              cudaStream_t s) {
+  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
+  tc_gemm_kernel<Cfg><<<grid, kNumThreads, Plan::TOTAL, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p, int grid,
+                                cudaStream_t s) {
+  return p.bias ? launch_cfg<FwdCfg<true>>(tm_h, tm_w, p, grid, s) : launch_cfg<FwdCfg<false>>(tm_h, tm_w, p, grid, s);
+}
+
+cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s) {
+  const int threads = 256;
+  const int blocks = (p.N + threads - 1) / threads;
+  fwd_merge_kernel<<<blocks, threads, 0, s>>>(p, out_logp, out_lse);
+  return cudaGetLastError();
+}
+
+}  // namespace llp

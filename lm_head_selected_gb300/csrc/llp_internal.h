@@ -1,0 +1,75 @@
+// Internal (non-exported) declarations shared by the kernel translation units
+// and the C-ABI layer.  Plain structs only: they are kernel parameters.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace llp {
+
+// Fixed tiling.  None of these depend on N, so each token row sees the same
+// vocab tiles, vocab splits, K order and merge order at every batch size.
+constexpr int kTileM = 128;           // tokens (or vocab rows for grad_weight) per tile
+constexpr int kTileN = 256;           // vocab (or hidden) columns per tile
+constexpr int kTileK = 64;            // K elements per pipeline stage
+constexpr int kTilesPerSplit = 2;     // forward vocab split = 512 columns
+constexpr int kSplitWidth = kTileN * kTilesPerSplit;
+constexpr int kKSegment = 32768;      // fixed K segment of the gradient GEMMs
+constexpr int kGroupM = 64;           // L2 raster group (M tiles); scheduling only
+
+struct FwdParams {
+  int N, D, V;
+  int num_m, num_splits, num_vt, group_m;
+  const float* bias;
+  const long long* targets;
+  const float* temperature;
+  long long ignore_index;
+  float* part_m;   // [num_splits][N] running max of each split
+  float* part_s;   // [num_splits][N] sum of exp(z - part_m) over the split
+  float* zt;       // [N] target logit (written by the split that holds the target)
+  unsigned int* err;
+};
+
+struct DzParams {
+  int N, D, V, V_pad;
+  int num_m, num_vt, group_m;
+  const float* bias;
+  const long long* targets;
+  const float* temperature;
+  long long ignore_index;
+  const float* grad_logp;
+  const float* lse;
+  __nv_bfloat16* dz;  // [N][V_pad]
+  float* gb_part;     // [num_m*4][V]: per 32-row block column sums of dz (bias only)
+  unsigned int* err;
+};
+
+struct GradGemmParams {
+  int rows;          // M extent: N for grad_hidden, V for grad_weight
+  int D;             // output columns
+  int K;             // reduction extent: V for grad_hidden, N for grad_weight
+  int num_m, num_d, nseg, kseg_blocks;
+  __nv_bfloat16* out;  // [rows][D] bf16 when nseg == 1
+  float* part;         // [nseg][rows][D] fp32 partials when nseg > 1
+  unsigned int* err;
+};
+
+// Launchers (return the launch error, never synchronise).
+cudaError_t fwd_setup();
+cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p, int grid,
+                                cudaStream_t s);
+cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s);
+
+cudaError_t bwd_setup();
+cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, int grid,
+                           cudaStream_t s);
+cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const GradGemmParams& p,
+                               int grid, cudaStream_t s);
+cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const GradGemmParams& p,
+                               int grid, cudaStream_t s);
+cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s);
+
+}  // namespace llp
