@@ -114,6 +114,24 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
 /* Human-readable name of a status code (static storage). */
 const char* linear_logp_status_string(int status);
 
+/*
+ * Optional launch recorder (a measurement aid; off by default, not
+ * thread-safe against concurrent calls).  While it is on, every forward /
+ * backward call records one CUDA event on its stream when it starts and one
+ * after each kernel it launches, so the time between consecutive events is the
+ * device time of one launch.
+ *   linear_logp_profile_start(capacity): clears the record and turns it on for
+ *     at most `capacity` launches (creates the events on first use).
+ *   linear_logp_profile_stop(kernel_ids, ms, capacity): turns it off,
+ *     synchronises the recorded events, writes up to `capacity` (kernel id,
+ *     milliseconds) pairs in launch order and returns how many launches were
+ *     recorded (or a negative LLP_ERR_* code).
+ *   linear_logp_kernel_name(id): name of a kernel id.
+ */
+int linear_logp_profile_start(int capacity);
+int linear_logp_profile_stop(int* kernel_ids, float* ms, int capacity);
+const char* linear_logp_kernel_name(int kernel_id);
+
 /* Synchronises `stream`, then reads and clears the current device's kernel
  * status word.  Returns LLP_OK if no kernel gave up on a wait since the last
  * call, LLP_ERR_DEVICE_TIMEOUT if one did (the detailed code goes to

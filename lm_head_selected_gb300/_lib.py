@@ -27,6 +27,9 @@ EXPORTED = (
     "linear_logp_bwd",
     "linear_logp_status_string",
     "linear_logp_device_status",
+    "linear_logp_profile_start",
+    "linear_logp_profile_stop",
+    "linear_logp_kernel_name",
 )
 
 _lock = threading.Lock()
@@ -74,6 +77,13 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_status_string.restype = ctypes.c_char_p
         lib.linear_logp_device_status.argtypes = [_p, ctypes.POINTER(ctypes.c_uint)]
         lib.linear_logp_device_status.restype = ctypes.c_int
+        lib.linear_logp_profile_start.argtypes = [ctypes.c_int]
+        lib.linear_logp_profile_start.restype = ctypes.c_int
+        lib.linear_logp_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float),
+                                                 ctypes.c_int]
+        lib.linear_logp_profile_stop.restype = ctypes.c_int
+        lib.linear_logp_kernel_name.argtypes = [ctypes.c_int]
+        lib.linear_logp_kernel_name.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -85,3 +95,19 @@ def status_string(status: int) -> str:
 def check(fn: str, status: int) -> None:
     if status != LLP_OK:
         raise LinearLogpError(fn, status, status_string(status))
+
+
+def profile_start(capacity: int) -> None:
+    check("linear_logp_profile_start", load().linear_logp_profile_start(int(capacity)))
+
+
+def profile_stop(capacity: int):
+    """Returns [(kernel name, milliseconds), ...] in launch order."""
+    lib = load()
+    ids = (ctypes.c_int * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = lib.linear_logp_profile_stop(ids, ms, capacity)
+    if n < 0:
+        check("linear_logp_profile_stop", n)
+    n = min(n, capacity)
+    return [(lib.linear_logp_kernel_name(ids[i]).decode(), float(ms[i])) for i in range(n)]

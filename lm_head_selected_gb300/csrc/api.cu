@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "linear_logp.h"
 #include "llp_internal.h"
@@ -170,6 +171,50 @@ int grid_for(int64_t units, int num_sms) {
   return static_cast<int>(units < num_sms ? units : num_sms);
 }
 
+// ----------------------------------------------------------------------------
+// Optional launch recorder (see linear_logp_profile_start in the header).
+// ----------------------------------------------------------------------------
+enum KernelId {
+  kKFwdPartials = 0,
+  kKFwdMerge,
+  kKDlogits,
+  kKGradHidden,
+  kKGradWeight,
+  kKSegSumHidden,
+  kKSegSumWeight,
+  kKBiasSum,
+  kKNumKernels
+};
+
+const char* const kKernelNames[kKNumKernels] = {"fwd_partials",  "fwd_merge",          "dlogits",
+                                                "grad_hidden",   "grad_weight",        "segment_sum_hidden",
+                                                "segment_sum_weight", "bias_sum"};
+
+struct Recorder {
+  std::mutex mu;
+  bool on = false;
+  int launch_cap = 0;
+  int launches = 0;
+  int used = 0;
+  std::vector<cudaEvent_t> events;
+  std::vector<int> ids;  // -1: call start; otherwise the kernel id launched just before
+};
+
+Recorder g_rec;
+
+void rec_mark(cudaStream_t s, int id) {
+  if (!g_rec.on) return;
+  std::lock_guard<std::mutex> lock(g_rec.mu);
+  if (!g_rec.on || g_rec.used >= static_cast<int>(g_rec.events.size())) return;
+  if (id >= 0) {
+    if (g_rec.launches >= g_rec.launch_cap) return;
+    ++g_rec.launches;
+  }
+  cudaEventRecord(g_rec.events[g_rec.used], s);
+  g_rec.ids[g_rec.used] = id;
+  ++g_rec.used;
+}
+
 }  // namespace
 
 extern "C" {
@@ -241,8 +286,11 @@ int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, c
   p.err = dev->status_ptr;
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
+  rec_mark(s, -1);
   if (llp::launch_fwd_partials(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+  rec_mark(s, kKFwdPartials);
   if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+  rec_mark(s, kKFwdMerge);
   return LLP_OK;
 }
 
@@ -310,7 +358,9 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     p.gb_part = want_gb ? reinterpret_cast<float*>(ws + L.gb_part) : nullptr;
     p.err = dev->status_ptr;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
+    rec_mark(s, -1);
     if (llp::launch_dlogits(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+    rec_mark(s, kKDlogits);
   }
 
   // B2: grad_hidden = dz . W over fixed vocab segments
@@ -332,9 +382,12 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     if (llp::launch_grad_hidden(tm_dz, tm_w_mn, p, grid_for(units, dev->num_sms), s) != cudaSuccess)
       return LLP_ERR_CUDA;
-    if (p.nseg > 1 &&
-        llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+    rec_mark(s, kKGradHidden);
+    if (p.nseg > 1) {
+      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s) != cudaSuccess)
+        return LLP_ERR_CUDA;
+      rec_mark(s, kKSegSumHidden);
+    }
   }
 
   // B3: grad_weight = dz^T . h over fixed token segments
@@ -356,9 +409,12 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, p, grid_for(units, dev->num_sms), s) != cudaSuccess)
       return LLP_ERR_CUDA;
-    if (p.nseg > 1 &&
-        llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+    rec_mark(s, kKGradWeight);
+    if (p.nseg > 1) {
+      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s) != cudaSuccess)
+        return LLP_ERR_CUDA;
+      rec_mark(s, kKSegSumWeight);
+    }
   }
 
   // B4: grad_bias
@@ -367,6 +423,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
                              s) != cudaSuccess)
       return LLP_ERR_CUDA;
+    rec_mark(s, kKBiasSum);
   }
   return LLP_OK;
 }
@@ -385,6 +442,47 @@ int linear_logp_device_status(void* stream, unsigned int* device_code) {
     return LLP_ERR_DEVICE_TIMEOUT;
   }
   return LLP_OK;
+}
+
+int linear_logp_profile_start(int capacity) {
+  if (capacity < 1) return LLP_ERR_BAD_SHAPE;
+  std::lock_guard<std::mutex> lock(g_rec.mu);
+  const size_t need = static_cast<size_t>(capacity) * 2 + 2;
+  while (g_rec.events.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return LLP_ERR_CUDA;
+    g_rec.events.push_back(e);
+  }
+  g_rec.ids.assign(g_rec.events.size(), -1);
+  g_rec.launch_cap = capacity;
+  g_rec.launches = 0;
+  g_rec.used = 0;
+  g_rec.on = true;
+  return LLP_OK;
+}
+
+int linear_logp_profile_stop(int* kernel_ids, float* ms, int capacity) {
+  std::lock_guard<std::mutex> lock(g_rec.mu);
+  g_rec.on = false;
+  if (g_rec.used == 0) return 0;
+  if (cudaEventSynchronize(g_rec.events[g_rec.used - 1]) != cudaSuccess) return LLP_ERR_CUDA;
+  int n = 0;
+  for (int i = 1; i < g_rec.used; ++i) {
+    if (g_rec.ids[i] < 0) continue;
+    if (n < capacity && kernel_ids != nullptr && ms != nullptr) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, g_rec.events[i - 1], g_rec.events[i]) != cudaSuccess) return LLP_ERR_CUDA;
+      kernel_ids[n] = g_rec.ids[i];
+      ms[n] = t;
+    }
+    ++n;
+  }
+  return n;
+}
+
+const char* linear_logp_kernel_name(int kernel_id) {
+  if (kernel_id < 0 || kernel_id >= kKNumKernels) return "unknown";
+  return kKernelNames[kernel_id];
 }
 
 }  // extern "C"

@@ -1,0 +1,135 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark
+times: every forward row checked for validity, sampled rows against the FP64
+oracle, grad_weight checked in full on a batch whose active rows the oracle
+can afford (all other rows ignored, so the full-size GEMMs still run over
+every token), and bitwise repeatability."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_helpers import (GW_ATOL, GW_RTOL, assert_close, check_backward, check_device_status, check_forward,
+                            gpu_bwd, gpu_fwd, np64, oracle_args, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from lm_head_selected_gb300 import build
+    build.build()
+
+
+def _sample_rows(N, k, seed, must=()):
+    g = torch.Generator().manual_seed(seed)
+    rows = set(torch.randperm(N, generator=g)[:k].tolist()) | set(must)
+    return sorted(rows)
+
+
+def _forward_properties(logp, lse, inp):
+    valid = torch.as_tensor(oracle.valid_rows(inp.targets.numpy(), inp.V, inp.ignore_index)).cuda()
+    assert torch.all(torch.isfinite(logp))
+    assert torch.all(logp[valid] <= 5e-3)
+    assert torch.all(logp[~valid] == 0)
+    assert torch.all(torch.isfinite(lse[valid])) and torch.all(torch.isneginf(lse[~valid]))
+
+
+def _sparse_targets(inp, active, seed):
+    """Same inputs, but only `active` rows keep their target; the rest are ignored."""
+    g = torch.Generator().manual_seed(seed)
+    keep = torch.randperm(inp.N, generator=g)[:active]
+    t = torch.full_like(inp.targets, -100)
+    t[keep] = inp.targets[keep]
+    out = inp.rows(torch.arange(inp.N))
+    out.targets = t
+    return out
+
+
+def test_rl_scoring_forward_full_size():
+    """N=16384, D=2688, V=131072 (batch 32 x seq 512), high-probability targets."""
+    inp = workloads.rl_scoring(seed=1002)
+    d = to_device(inp)
+    logp, lse = gpu_fwd(d)
+    check_device_status()
+    _forward_properties(logp, lse, inp)
+    rows = _sample_rows(inp.N, 192, 1, must=(0, inp.N - 1))
+    check_forward(inp, logp, lse, rows=rows)
+    # the planted targets are high-probability tokens: median logp well above -log V
+    valid = torch.as_tensor(oracle.valid_rows(inp.targets.numpy(), inp.V, -100)).cuda()
+    assert float(logp[valid].median()) > -4.0
+    logp2, lse2 = gpu_fwd(d)
+    assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
+
+
+def test_rl_head_fwd_bwd_full_size():
+    """The benchmark's step (N=16384, D=2688, V=131072, grad_logp ~ N(0,1)): sampled
+    grad_hidden rows, full grad_weight on a batch with 192 active rows."""
+    inp = workloads.rl_scoring(seed=1002, grad_std=1.0)
+    d = to_device(inp)
+    logp, lse = gpu_fwd(d)
+    gh, gw, _ = gpu_bwd(d, lse)
+    check_device_status()
+    rows = _sample_rows(inp.N, 96, 2, must=(0, inp.N - 1))
+    check_backward(inp, gh, None, None, rows=rows)
+    gh2, gw2, _ = gpu_bwd(d, lse)
+    assert torch.equal(gh, gh2) and torch.equal(gw, gw2)
+    del gw, gw2, gh2
+    sp = _sparse_targets(inp, 192, 3)
+    ds = to_device(sp)
+    lp_s, lse_s = gpu_fwd(ds)
+    _, gw_s, _ = gpu_bwd(ds, lse_s, need_hidden=False)
+    check_device_status()
+    check_backward(sp, None, gw_s, None)
+
+
+def test_train_step_full_size():
+    """N=16384, D=4096, V=128256 with bias: sampled rows of logp / grad_hidden,
+    grad_weight / grad_bias in full on a batch with 128 active rows."""
+    inp = workloads.train()
+    d = to_device(inp)
+    logp, lse = gpu_fwd(d)
+    gh, gw, gb = gpu_bwd(d, lse)
+    check_device_status()
+    _forward_properties(logp, lse, inp)
+    rows = _sample_rows(inp.N, 96, 4, must=(inp.N - 1,))
+    check_forward(inp, logp, lse, rows=rows)
+    check_backward(inp, gh, None, None, rows=rows)
+    assert torch.all(torch.isfinite(gb))
+    del gw, gh
+    sp = _sparse_targets(inp, 128, 5)
+    ds = to_device(sp)
+    lp_s, lse_s = gpu_fwd(ds)
+    _, gw_s, gb_s = gpu_bwd(ds, lse_s, need_hidden=False)
+    check_device_status()
+    check_backward(sp, None, gw_s, gb_s)
+
+
+def test_long_context_full_size():
+    """N=65600 (3 token segments for grad_weight), one row shifted by +9984, duplicate
+    targets; two runs bitwise identical; grad_weight in full on 96 active rows."""
+    inp = workloads.long_context()
+    d = to_device(inp)
+    logp, lse = gpu_fwd(d)
+    gh, gw, _ = gpu_bwd(d, lse)
+    check_device_status()
+    _forward_properties(logp, lse, inp)
+    rows = _sample_rows(inp.N, 96, 6, must=(0, 1, 64, inp.N - 1))
+    check_forward(inp, logp, lse, rows=rows)
+    check_backward(inp, gh, None, None, rows=rows)
+    logp2, lse2 = gpu_fwd(d)
+    gh2, gw2, _ = gpu_bwd(d, lse2)
+    assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
+    assert torch.equal(gh, gh2) and torch.equal(gw, gw2)
+    del gw, gw2, gh, gh2
+    # the shifted row agrees with its unshifted twin
+    twin = inp.rows(torch.tensor([0]))
+    twin.hidden[0, -1] = 0
+    lp_t, _ = gpu_fwd(to_device(twin))
+    assert abs(float(lp_t[0]) - float(logp[0])) < 5e-3
+    sp = _sparse_targets(inp, 96, 7)
+    ds = to_device(sp)
+    lp_s, lse_s = gpu_fwd(ds)
+    _, gw_s, _ = gpu_bwd(ds, lse_s, need_hidden=False)
+    check_device_status()
+    check_backward(sp, None, gw_s, None)

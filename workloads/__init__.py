@@ -145,10 +145,12 @@ def rl_scoring(N: int = 16384, D: int = 2688, V: int = 131072, seed: int = 1002,
 
     Target mix: 85% high-probability tokens, 10% uniform tokens, 5% ignore index.
     A high-probability target t is planted by adding gamma * W[t] / (D * 0.02^2) to
-    the row's hidden state (gamma ~ U[4, 9]), which lifts that token's logit by about
-    gamma above the N(0, ~1) background, so the token sits at or near the top of the
-    row's distribution.  This draws such tokens without computing any logits or
-    softmax here.  grad_logp ~ N(0, 1) so the same batch also serves a training step.
+    the row's hidden state (gamma ~ U[11, 17]), which lifts that token's logit by about
+    gamma above the N(0, ~1) background.  The background's log-mass is about
+    log(V) + 1/2 = 12.3, so the planted token carries most of the row's probability
+    (log-prob roughly -1.5 .. 0), as a token sampled from the model itself would.
+    This draws such tokens without computing any logits or softmax here.
+    grad_logp ~ N(0, 1) so the same batch also serves a training step.
     """
     g = _gen(seed)
     w_std = 0.02
@@ -158,7 +160,7 @@ def rl_scoring(N: int = 16384, D: int = 2688, V: int = 131072, seed: int = 1002,
     kind = torch.rand(N, generator=g)
     planted = kind < 0.85
     ignored = kind >= 0.95
-    gamma = 4.0 + 5.0 * torch.rand(N, generator=g)
+    gamma = 11.0 + 6.0 * torch.rand(N, generator=g)
     rows = torch.nonzero(planted).flatten()
     step = 4096
     for s in range(0, rows.numel(), step):
