@@ -66,7 +66,8 @@ enum {
   LLP_ERR_UNSUPPORTED_DEVICE = -4,  /* the current device is not an sm_103 GPU */
   LLP_ERR_WORKSPACE_TOO_SMALL = -5, /* workspace_bytes below the *_workspace_bytes() query */
   LLP_ERR_CUDA = -6,                /* a CUDA runtime / driver call or launch failed */
-  LLP_ERR_DEVICE_TIMEOUT = -7       /* a kernel gave up on a wait (see linear_logp_device_status) */
+  LLP_ERR_DEVICE_TIMEOUT = -7,      /* a kernel gave up on a wait (see linear_logp_device_status) */
+  LLP_ERR_SCRATCH_LIMIT = -8        /* problem too large for linear_logp_fwd_noalloc's fixed scratch */
 };
 
 /* Bytes of workspace linear_logp_fwd needs for an N x D x V problem
@@ -95,6 +96,39 @@ size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_
 int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
                     const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
                     float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Forward that allocates nothing and takes no workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory on their own: a plugin inside a host
+ * program that owns all device memory through its own allocator and hands
+ * none out, a service that has already reserved the whole device (weights,
+ * caches) and forbids further allocation, or a latency-critical loop where
+ * cudaMalloc is not allowed because it is slow and may synchronise the device.
+ *
+ * Same arguments, results and checks as linear_logp_fwd, minus the workspace.
+ * The scratch (per-split max / sum pairs and target logits) lives in one
+ * file-scope device array of LINEAR_LOGP_NOALLOC_SCRATCH_BYTES (16 MiB) inside
+ * the library; every GPU that loads the library holds it until the process
+ * exits.  The problem needs about N * (8 * ceil(V / 512) + 4) bytes of it (plus
+ * 256-byte alignment of each region): up to about 8000 tokens at V = 131072.
+ * Larger problems return LLP_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   - No cudaMalloc / cudaFree or any allocating call is made.
+ *   - The first call on a device performs a one-time set-up with that device
+ *     current (it looks up the array's device address); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it has to start at zero, because every call writes each
+ *     scratch entry it later reads.  Calls whose work overlaps on the GPU
+ *     (different streams or threads without ordering between them) race on
+ *     the array and give undefined results: order them on one stream or with
+ *     events.
+ */
+#define LINEAR_LOGP_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                            const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                            float* out_logp, float* out_lse, void* stream);
 
 /*
  * Backward.  Same inputs as the forward plus

@@ -30,7 +30,9 @@ EXPORTED = (
     "linear_logp_profile_start",
     "linear_logp_profile_stop",
     "linear_logp_kernel_name",
+    "linear_logp_fwd_noalloc",
 )
+LLP_ERR_SCRATCH_LIMIT = -8
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +86,8 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_profile_stop.restype = ctypes.c_int
         lib.linear_logp_kernel_name.argtypes = [ctypes.c_int]
         lib.linear_logp_kernel_name.restype = ctypes.c_char_p
+        lib.linear_logp_fwd_noalloc.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _p, _p]
+        lib.linear_logp_fwd_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 

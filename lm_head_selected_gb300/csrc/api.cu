@@ -239,6 +239,8 @@ const char* linear_logp_status_string(int status) {
     case LLP_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case LLP_ERR_CUDA: return "CUDA call or kernel launch failed";
     case LLP_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case LLP_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than linear_logp_fwd_noalloc's fixed 16 MiB array holds";
     default: return "unknown status";
   }
 }
@@ -441,6 +443,81 @@ int linear_logp_device_status(void* stream, unsigned int* device_code) {
     if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return LLP_ERR_CUDA;
     return LLP_ERR_DEVICE_TIMEOUT;
   }
+  return LLP_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Forward without a caller workspace (linear_logp_fwd_noalloc in the header):
+// for callers that cannot allocate device memory themselves.  Its scratch is
+// this fixed file-scope array; host code only ever uses the device address
+// obtained from cudaGetSymbolAddress, never the array's name.
+// ----------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LINEAR_LOGP_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[kMaxDevices] = {};
+
+// One-time per-device look-up of the scratch array's device address, with that
+// device current.  Returns LLP_OK and the address, or LLP_ERR_CUDA.
+static int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LLP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LLP_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return LLP_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return LLP_OK;
+}
+
+int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                            const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                            float* out_logp, float* out_lse, void* stream) {
+  int st = check_shapes(N, D, V);
+  if (st != LLP_OK) return st;
+  if (N == 0) return LLP_OK;
+  st = check_inputs(hidden, weight, bias, targets, temperature, N, D, V);
+  if (st != LLP_OK) return st;
+  if (out_logp == nullptr || out_lse == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(out_logp, 4) || !aligned(out_lse, 4)) return LLP_ERR_MISALIGNED;
+  const FwdLayout L = fwd_layout(N, V);
+  if (L.total > static_cast<size_t>(LINEAR_LOGP_NOALLOC_SCRATCH_BYTES)) return LLP_ERR_SCRATCH_LIMIT;
+
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != LLP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap tm_h, tm_w;
+  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kTileN) != LLP_OK) return LLP_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  llp::FwdParams p;
+  p.N = static_cast<int>(N);
+  p.D = static_cast<int>(D);
+  p.V = static_cast<int>(V);
+  p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+  p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
+  p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
+  p.group_m = llp::kGroupM;
+  p.bias = bias;
+  p.targets = reinterpret_cast<const long long*>(targets);
+  p.temperature = temperature;
+  p.ignore_index = ignore_index;
+  p.part_m = reinterpret_cast<float*>(ws + L.part_m);
+  p.part_s = reinterpret_cast<float*>(ws + L.part_s);
+  p.zt = reinterpret_cast<float*>(ws + L.zt);
+  p.err = dev->status_ptr;
+
+  const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
   return LLP_OK;
 }
 

@@ -106,6 +106,27 @@ def linear_logp_fwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.T
     return logp, lse
 
 
+def linear_logp_fwd_noalloc(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                            bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
+                            ignore_index: int = IGNORE_INDEX,
+                            out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """Forward through ``linear_logp_fwd_noalloc``: no workspace, for callers that
+    cannot allocate device memory themselves (the library uses its own fixed
+    16 MiB device array; pass preallocated ``out`` buffers to allocate nothing
+    here either).  Calls that overlap on the GPU share that array and race."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    lib = _lib.load()
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    else:
+        logp, lse = out
+    st = lib.linear_logp_fwd_noalloc(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), _ptr(temperature),
+                                     N, D, V, int(ignore_index), _ptr(logp), _ptr(lse), _stream(dev))
+    _lib.check("linear_logp_fwd_noalloc", st)
+    return logp, lse
+
+
 def linear_logp_bwd(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hidden: torch.Tensor,
                     weight: torch.Tensor, targets: torch.Tensor, bias: Optional[torch.Tensor] = None,
                     temperature: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,

@@ -1,0 +1,92 @@
+"""The forward entry point that allocates nothing (linear_logp_fwd_noalloc).
+
+It is meant for callers that cannot allocate device memory themselves, such as
+a plugin inside a host program that owns every byte of device memory, or a
+loop where cudaMalloc is not allowed.  Its scratch is a fixed 16 MiB array
+inside the library, shared by every call.  These tests call it through the C
+ABI and check that two calls in a row agree with the regular forward (which
+takes a caller workspace), that a problem too large for the array is refused
+before anything runs, and that the array's leftover contents from a previous
+call do not leak into the next one.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it passes alone in a fresh process too.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity_helpers import LOGP_ATOL, LSE_ATOL, check_device_status, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lm_head_selected_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def _noalloc(lib, d, N, D, V):
+    dev = d["hidden"].device
+    logp = torch.full((N,), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((N,), float("nan"), dtype=torch.float32, device=dev)
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = lib.linear_logp_fwd_noalloc(p(d["hidden"]), p(d["weight"]), p(d["bias"]), p(d["targets"]),
+                                     p(d["temperature"]), N, D, V, d["ignore_index"], p(logp), p(lse),
+                                     ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    return st, logp, lse
+
+
+def _regular(d):
+    import lm_head_selected_gb300 as llp
+    return llp.linear_logp_fwd(d["hidden"], d["weight"], d["targets"], d["bias"], d["temperature"],
+                               d["ignore_index"])
+
+
+def _agree(a, b, atol):
+    a = a.double().cpu().numpy()
+    b = b.double().cpu().numpy()
+    assert np.array_equal(np.isfinite(a), np.isfinite(b))
+    fin = np.isfinite(b)
+    assert np.all(np.abs(a[fin] - b[fin]) <= atol)
+    assert np.array_equal(a[~fin], b[~fin])
+
+
+CASES = [
+    # (N, D, V, bias, temperature): the Nemotron head near the scratch limit, then a
+    # smaller ragged problem, so the second call runs on the first call's leftovers.
+    (4000, 2688, 131072, False, True),
+    (333, 264, 50257, True, False),
+]
+
+
+def test_two_calls_in_a_row_match_the_workspace_forward(lib):
+    for i, (N, D, V, bias, temp) in enumerate(CASES):
+        inp = workloads.make_inputs(N, D, V, seed=500 + i, weight_std=2.0 / math.sqrt(D),
+                                    bias_std=0.3 if bias else None,
+                                    temperature_range=(0.7, 1.3) if temp else None, n_ignore=7, n_out_of_range=3)
+        d = to_device(inp)
+        st, logp, lse = _noalloc(lib, d, N, D, V)
+        assert st == 0, lib.linear_logp_status_string(st)
+        ref_logp, ref_lse = _regular(d)
+        check_device_status()
+        _agree(logp, ref_logp, LOGP_ATOL)
+        _agree(lse, ref_lse, LSE_ATOL)
+
+
+def test_refuses_problems_beyond_the_scratch_limit(lib):
+    from lm_head_selected_gb300 import _lib
+    N, D, V = 9000, 2688, 131072  # needs about 18.5 MB > 16 MiB
+    inp = workloads.make_inputs(N, D, 1024, seed=3)  # small weight: only the sizes matter here
+    d = to_device(inp)
+    w = torch.empty((V, D), dtype=torch.bfloat16, device="cuda")
+    d["weight"] = w
+    st, logp, lse = _noalloc(lib, d, N, D, V)
+    assert st == _lib.LLP_ERR_SCRATCH_LIMIT
+    assert torch.all(torch.isnan(logp)) and torch.all(torch.isnan(lse))  # nothing ran
