@@ -21,6 +21,7 @@ struct DeviceInit {
   int status = LLP_OK;
   int num_sms = 0;
   unsigned int* status_ptr = nullptr;
+  llp::LaunchCaps caps = {};
 };
 
 std::mutex g_mu;
@@ -60,7 +61,7 @@ int init_device(DeviceInit** out) {
     }
     if (major != 10 || minor != 3) {
       d.status = LLP_ERR_UNSUPPORTED_DEVICE;
-    } else if (llp::fwd_setup() != cudaSuccess || llp::bwd_setup() != cudaSuccess ||
+    } else if (llp::fwd_setup(&d.caps) != cudaSuccess || llp::bwd_setup(&d.caps) != cudaSuccess ||
                cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_ptr), g_status_word) != cudaSuccess) {
       d.status = LLP_ERR_CUDA;
     } else {
@@ -87,12 +88,12 @@ int check_shapes(int64_t N, int64_t D, int64_t V) {
   if (N > kLim31 || D > kLim31 || V > kLim31) return LLP_ERR_BAD_SHAPE;
   if (!product_ok(N, D) || !product_ok(V, D) || !product_ok(N, round_up(V, 64))) return LLP_ERR_BAD_SHAPE;
   // every work-unit count and tile index must fit a 32-bit int
-  const int64_t num_m = cdiv(N, llp::kTileM);
+  const int64_t num_m = cdiv(N, llp::kUnitM);
   const int64_t num_vt = cdiv(V, llp::kTileN);
   const int64_t num_d = cdiv(D, llp::kTileN);
   if (num_m * num_vt > kLim31) return LLP_ERR_BAD_SHAPE;
   if (cdiv(V, llp::kKSegment) * num_m * num_d > kLim31) return LLP_ERR_BAD_SHAPE;
-  if (cdiv(N, llp::kKSegment) * cdiv(V, llp::kTileM) * num_d > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (cdiv(N, llp::kKSegment) * cdiv(V, llp::kUnitM) * num_d > kLim31) return LLP_ERR_BAD_SHAPE;
   return LLP_OK;
 }
 
@@ -139,14 +140,14 @@ struct BwdLayout {
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, bool want_dw) {
   const size_t V_pad = round_up(static_cast<size_t>(V), 64);
-  const size_t num_m = static_cast<size_t>(cdiv(N, llp::kTileM));
+  const size_t num_m = static_cast<size_t>(cdiv(N, llp::kUnitM));
   const size_t nseg_v = static_cast<size_t>(cdiv(V, llp::kKSegment));
   const size_t nseg_n = static_cast<size_t>(cdiv(N, llp::kKSegment));
   Carver c;
   BwdLayout L;
   L.dz = c.take(static_cast<size_t>(N) * V_pad * 2);
   L.has_gb = bias;
-  L.gb_part = bias ? c.take(num_m * 4 * static_cast<size_t>(V) * sizeof(float)) : 0;
+  L.gb_part = bias ? c.take(num_m * (llp::kUnitM / 32) * static_cast<size_t>(V) * sizeof(float)) : 0;
   L.has_dh = want_dh && nseg_v > 1;
   L.dh_part = L.has_dh ? c.take(nseg_v * static_cast<size_t>(N) * D * sizeof(float)) : 0;
   L.has_dw = want_dw && nseg_n > 1;
@@ -165,10 +166,6 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
-}
-
-int grid_for(int64_t units, int num_sms) {
-  return static_cast<int>(units < num_sms ? units : num_sms);
 }
 
 // ----------------------------------------------------------------------------
@@ -267,14 +264,14 @@ int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, c
 
   CUtensorMap tm_h, tm_w;
   if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kTileN) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
   p.V = static_cast<int>(V);
-  p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+  p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
   p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
   p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
   p.group_m = llp::kGroupM;
@@ -289,7 +286,7 @@ int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, c
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   rec_mark(s, -1);
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
   rec_mark(s, kKFwdPartials);
   if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
   rec_mark(s, kKFwdMerge);
@@ -341,13 +338,13 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
   {
     CUtensorMap tm_h, tm_w;
     if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kTileN) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
     p.V = static_cast<int>(V);
     p.V_pad = static_cast<int>(V_pad);
-    p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
     p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
     p.group_m = llp::kGroupM;
     p.bias = bias;
@@ -361,7 +358,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     p.err = dev->status_ptr;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
-    if (llp::launch_dlogits(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+    if (llp::launch_dlogits(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
     rec_mark(s, kKDlogits);
   }
 
@@ -374,7 +371,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     p.rows = static_cast<int>(N);
     p.D = static_cast<int>(D);
     p.K = static_cast<int>(V);
-    p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
     p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
     p.nseg = static_cast<int>(cdiv(V, llp::kKSegment));
     p.kseg_blocks = llp::kKSegment / llp::kTileK;
@@ -382,7 +379,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
     p.err = dev->status_ptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
-    if (llp::launch_grad_hidden(tm_dz, tm_w_mn, p, grid_for(units, dev->num_sms), s) != cudaSuccess)
+    if (llp::launch_grad_hidden(tm_dz, tm_w_mn, p, units, dev->caps, s) != cudaSuccess)
       return LLP_ERR_CUDA;
     rec_mark(s, kKGradHidden);
     if (p.nseg > 1) {
@@ -401,7 +398,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
     p.K = static_cast<int>(N);
-    p.num_m = static_cast<int>(cdiv(V, llp::kTileM));
+    p.num_m = static_cast<int>(cdiv(V, llp::kUnitM));
     p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
     p.nseg = static_cast<int>(cdiv(N, llp::kKSegment));
     p.kseg_blocks = llp::kKSegment / llp::kTileK;
@@ -409,7 +406,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
     p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
     p.err = dev->status_ptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
-    if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, p, grid_for(units, dev->num_sms), s) != cudaSuccess)
+    if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, p, units, dev->caps, s) != cudaSuccess)
       return LLP_ERR_CUDA;
     rec_mark(s, kKGradWeight);
     if (p.nseg > 1) {
@@ -421,7 +418,7 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
 
   // B4: grad_bias
   if (want_gb) {
-    const int nblocks = static_cast<int>(cdiv(N, llp::kTileM) * 4);
+    const int nblocks = static_cast<int>(cdiv(N, llp::kUnitM) * (llp::kUnitM / 32));
     if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
                              s) != cudaSuccess)
       return LLP_ERR_CUDA;
@@ -495,14 +492,14 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
 
   CUtensorMap tm_h, tm_w;
   if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kTileN) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
   p.V = static_cast<int>(V);
-  p.num_m = static_cast<int>(cdiv(N, llp::kTileM));
+  p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
   p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
   p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
   p.group_m = llp::kGroupM;
@@ -516,7 +513,7 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   p.err = dev->status_ptr;
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, grid_for(units, dev->num_sms), s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
   if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
   return LLP_OK;
 }

@@ -60,9 +60,11 @@ template <bool HAS_BIAS>
 struct DzCfg {
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
+  static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int EXTRA_SMEM = 0;
+  static constexpr int UM = kUnitM;
   using Params = DzParams;
 
   struct RowState {
@@ -85,7 +87,7 @@ struct DzCfg {
     const int vt = r / gm;
     const int mt = grp * p.group_m + (r - vt * gm);
     UnitInfo ui;
-    ui.m0 = mt * BM;
+    ui.m0 = mt * UM;
     ui.n0 = vt * BN;
     ui.ntiles = 1;
     ui.kb0 = 0;
@@ -112,11 +114,11 @@ struct DzCfg {
     }
   }
 
-  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int, int, int g, int lane,
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int, int row, int lane,
                                               uint32_t taddr, RowState& rs) {
     const int v0 = ui.n0;
     const bool full = (v0 + BN) <= p.V;
-    const int mt = ui.m0 / BM;
+    const int blk = (ui.m0 + row) >> 5;  // 32-row block of this warp
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float z[32];
@@ -162,7 +164,7 @@ struct DzCfg {
       if (HAS_BIAS && p.gb_part != nullptr) {  // warp-uniform
         const float colsum = warp_column_sums(z, lane);
         const int v = vc + lane;
-        if (v < p.V) p.gb_part[static_cast<size_t>(mt * 4 + g) * p.V + v] = colsum;
+        if (v < p.V) p.gb_part[static_cast<size_t>(blk) * p.V + v] = colsum;
       }
     }
   }
@@ -177,9 +179,11 @@ template <bool A_MN_, bool B_MN_>
 struct GradCfg {
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
+  static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int EXTRA_SMEM = 0;
+  static constexpr int UM = kUnitM;
   using Params = GradGemmParams;
 
   struct RowState {
@@ -201,7 +205,7 @@ struct GradCfg {
     const int dt = r - mt * p.num_d;
     const int total_kb = (p.K + BK - 1) / BK;
     UnitInfo ui;
-    ui.m0 = mt * BM;
+    ui.m0 = mt * UM;
     ui.n0 = dt * BN;
     ui.ntiles = 1;
     ui.kb0 = seg * p.kseg_blocks;
@@ -213,7 +217,7 @@ struct GradCfg {
     rs.r = ui.m0 + row;
   }
 
-  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int u, int, int, int, int,
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int u, int, int, int,
                                               uint32_t taddr, RowState& rs) {
     const int seg = u / (p.num_m * p.num_d);
 #pragma unroll 1
@@ -281,40 +285,34 @@ __global__ void __launch_bounds__(256) bias_sum_kernel(const float* __restrict__
 }
 
 template <class Cfg>
-static cudaError_t set_smem(void) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
-  return cudaFuncSetAttribute(tc_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan::TOTAL);
+static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p,
+                                long long units, int groups, cudaStream_t s) {
+  const long long g = units < groups ? units : groups;
+  return launch_gemm<Cfg>(a, b, p, static_cast<int>(g) * Plan<Cfg>::NCTA, s);
 }
 
-template <class Cfg>
-static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p, int grid,
-                              cudaStream_t s) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
-  tc_gemm_kernel<Cfg><<<grid, kNumThreads, Plan::TOTAL, s>>>(a, b, p);
-  return cudaGetLastError();
-}
-
-cudaError_t bwd_setup() {
+cudaError_t bwd_setup(LaunchCaps* caps) {
   cudaError_t e;
-  if ((e = set_smem<DzCfg<false>>()) != cudaSuccess) return e;
-  if ((e = set_smem<DzCfg<true>>()) != cudaSuccess) return e;
-  if ((e = set_smem<GradCfg<false, true>>()) != cudaSuccess) return e;
-  return set_smem<GradCfg<true, true>>();
+  if ((e = setup_gemm<DzCfg<false>>(&caps->dz_groups[0])) != cudaSuccess) return e;
+  if ((e = setup_gemm<DzCfg<true>>(&caps->dz_groups[1])) != cudaSuccess) return e;
+  if ((e = setup_gemm<GradCfg<false, true>>(&caps->gh_groups)) != cudaSuccess) return e;
+  return setup_gemm<GradCfg<true, true>>(&caps->gw_groups);
 }
 
-cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, int grid,
-                           cudaStream_t s) {
-  return p.bias ? launch_cfg<DzCfg<true>>(tm_h, tm_w, p, grid, s) : launch_cfg<DzCfg<false>>(tm_h, tm_w, p, grid, s);
+cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, long long units,
+                           const LaunchCaps& caps, cudaStream_t s) {
+  return p.bias ? launch_units<DzCfg<true>>(tm_h, tm_w, p, units, caps.dz_groups[1], s)
+                : launch_units<DzCfg<false>>(tm_h, tm_w, p, units, caps.dz_groups[0], s);
 }
 
 cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const GradGemmParams& p,
-                               int grid, cudaStream_t s) {
-  return launch_cfg<GradCfg<false, true>>(tm_dz, tm_w_mn, p, grid, s);
+                               long long units, const LaunchCaps& caps, cudaStream_t s) {
+  return launch_units<GradCfg<false, true>>(tm_dz, tm_w_mn, p, units, caps.gh_groups, s);
 }
 
 cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const GradGemmParams& p,
-                               int grid, cudaStream_t s) {
-  return launch_cfg<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, p, grid, s);
+                               long long units, const LaunchCaps& caps, cudaStream_t s) {
+  return launch_units<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, p, units, caps.gw_groups, s);
 }
 
 cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s) {

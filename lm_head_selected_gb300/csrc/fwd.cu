@@ -32,10 +32,12 @@ template <bool HAS_BIAS>
 struct FwdCfg {
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
+  static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int EXTRA_SMEM = 0;
   static constexpr int TPS = kTilesPerSplit;
+  static constexpr int UM = kUnitM;
   using Params = FwdParams;
 
   struct RowState {
@@ -62,7 +64,7 @@ struct FwdCfg {
     const int split = r / gm;
     const int mt = grp * p.group_m + (r - split * gm);
     UnitInfo ui;
-    ui.m0 = mt * BM;
+    ui.m0 = mt * UM;
     ui.n0 = split * TPS * BN;
     ui.ntiles = min(TPS, p.num_vt - split * TPS);
     ui.kb0 = 0;
@@ -84,7 +86,7 @@ struct FwdCfg {
     }
   }
 
-  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int j, int, int, int,
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int j, int, int,
                                               uint32_t taddr, RowState& rs) {
     const int v0 = ui.n0 + j * BN;
     const bool full = (v0 + BN) <= p.V;
@@ -170,29 +172,23 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __re
   out_logp[n] = (p.zt[n] - M) - ls;
 }
 
-template <class Cfg>
-static cudaError_t set_smem(void) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
-  return cudaFuncSetAttribute(tc_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan::TOTAL);
-}
-
-cudaError_t fwd_setup() {
-  cudaError_t e = set_smem<FwdCfg<false>>();
+cudaError_t fwd_setup(LaunchCaps* caps) {
+  cudaError_t e = setup_gemm<FwdCfg<false>>(&caps->fwd_groups[0]);
   if (e != cudaSuccess) return e;
-  return set_smem<FwdCfg<true>>();
+  return setup_gemm<FwdCfg<true>>(&caps->fwd_groups[1]);
 }
 
 template <class Cfg>
-static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p, int grid,
-                              cudaStream_t s) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
-  tc_gemm_kernel<Cfg><<<grid, kNumThreads, Plan::TOTAL, s>>>(a, b, p);
-  return cudaGetLastError();
+static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p,
+                                long long units, int groups, cudaStream_t s) {
+  const long long g = units < groups ? units : groups;
+  return launch_gemm<Cfg>(a, b, p, static_cast<int>(g) * Plan<Cfg>::NCTA, s);
 }
 
-cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p, int grid,
-                                cudaStream_t s) {
-  return p.bias ? launch_cfg<FwdCfg<true>>(tm_h, tm_w, p, grid, s) : launch_cfg<FwdCfg<false>>(tm_h, tm_w, p, grid, s);
+cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,
+                                long long units, const LaunchCaps& caps, cudaStream_t s) {
+  return p.bias ? launch_units<FwdCfg<true>>(tm_h, tm_w, p, units, caps.fwd_groups[1], s)
+                : launch_units<FwdCfg<false>>(tm_h, tm_w, p, units, caps.fwd_groups[0], s);
 }
 
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s) {

@@ -1,20 +1,30 @@
 // Warp-specialised, persistent tcgen05 GEMM core shared by every contraction
 // of the fused linear log-prob path.
 //
-//   warp 0      : TMA producer (one elected lane) streaming A/B k-blocks into a
-//                 ring of shared-memory stages, completion on mbarriers.
-//   warp 1      : TMEM owner + MMA issuer (one elected lane): tcgen05.mma
-//                 128 x BN x 16 bf16 -> fp32 into one of two TMEM accumulators.
+//   warp 0      : TMA producer (one lane) streaming A/B k-blocks into a ring of
+//                 shared-memory stages, completion on mbarriers.
+//   warp 1      : TMEM owner; one lane issues tcgen05.mma 16-deep steps into one
+//                 of two fp32 TMEM accumulators (256 columns each).
 //   warps 2..5  : epilogue; warp w reads TMEM lanes 32*(w%4)..+31, so each
 //                 thread owns one accumulator row.  The epilogue of tile i
 //                 overlaps the MMAs of tile i+1 (double-buffered TMEM).
 //
-// A unit of work is a run of `ntiles` consecutive BM x BN output tiles that
-// share A rows (the forward's vocab split) or a single tile with a K range
-// (a fixed K segment of the gradient GEMMs).  CTAs take units round-robin;
-// which CTA runs a unit never changes any arithmetic, so results do not
-// depend on the grid size, and every per-row / per-element reduction runs
-// in a fixed order.
+// Two modes, chosen per configuration at compile time:
+//   single CTA (PAIR = false): a CTA computes 128 x BN tiles on its own SM.
+//   CTA pair   (PAIR = true) : a 2-CTA cluster computes 256 x BN tiles with
+//       tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA loads its
+//       own 128 rows of A and half (BN/2 rows) of B, so per CTA the shared
+//       memory and L2 operand traffic per MMA falls by a third.  Both CTAs'
+//       TMA loads complete on the even CTA's stage barrier; its commits are
+//       multicast to both CTAs; the odd CTA's epilogue warps release an
+//       accumulator with a remote arrive on the even CTA's barrier.
+//
+// A unit of work is a run of `ntiles` consecutive output tiles that share A
+// rows (the forward's vocab split) or a single tile with a K range (a fixed K
+// segment of the gradient GEMMs).  CTAs (or pairs) take units round-robin;
+// which one runs a unit never changes any arithmetic, so results do not depend
+// on the grid size, and every per-row / per-element reduction runs in a fixed
+// order.
 //
 // Operand layouts (both 128-byte swizzled, as TMA writes them):
 //   K-major  : box {64 K, R rows}; row pitch 128 B; 8-row groups 1024 B apart.
@@ -27,31 +37,37 @@
 
 namespace llp {
 
-constexpr int BM = kTileM;
+constexpr int BM = kTileM;  // accumulator rows per CTA
 constexpr int BK = kTileK;
 constexpr int UMMA_K = 16;
 constexpr int kNumThreads = 192;
-constexpr int kNumEpiThreads = 128;
 constexpr int kTmemCols = 512;
 
 struct UnitInfo {
-  int m0;      // first A row (M coordinate) of the unit
+  int m0;      // first A row (M coordinate) of the unit (of the pair in pair mode)
   int n0;      // N coordinate of the unit's first tile
   int ntiles;  // tiles along N, each BN wide
   int kb0;     // first k-block (BK elements each)
   int nkb;     // k-blocks per tile
 };
 
-template <int BN_, int STAGES_, int EXTRA_>
-struct SmemPlan {
+template <class Cfg>
+struct Plan {
+  static constexpr bool PAIR = Cfg::PAIR;
+  static constexpr int NCTA = PAIR ? 2 : 1;
+  static constexpr int UM = NCTA * BM;                         // unit rows (M) per tile
+  static constexpr int B_ROWS = PAIR ? Cfg::BN / 2 : Cfg::BN;  // B rows each CTA loads
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN_ * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int TILES_BYTES = STAGES_ * STAGE_BYTES;
-  static constexpr int BAR_OFFSET = TILES_BYTES + EXTRA_;
+  static constexpr uint32_t TX_BYTES = NCTA * STAGE_BYTES;  // bytes landing per stage on the MMA's barrier
+  static constexpr int TILES_BYTES = Cfg::STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFFSET = TILES_BYTES + Cfg::EXTRA_SMEM;
   static constexpr int BAR_BYTES = 256;
   static constexpr int TOTAL = BAR_OFFSET + BAR_BYTES + 1024;  // + alignment slack
+  static constexpr int EPI_ARRIVALS = 4 * NCTA;                // one per epilogue warp of the pair
   static_assert(TOTAL <= 232448, "shared memory budget exceeded");
+  static_assert(B_ROWS % 64 == 0 && B_ROWS <= 256, "B half must be whole 64-row swizzle atoms");
 };
 
 struct SharedState {
@@ -65,41 +81,66 @@ struct SharedState {
   uint8_t* tiles;
   uint8_t* extra;
   uint32_t tmem_base;
+  uint32_t rank;    // CTA rank inside the pair (0 in single-CTA mode)
+  int unit_first;   // first unit of this CTA (or pair)
+  int unit_stride;  // number of CTAs (or pairs) in the grid
 };
 
 // ----------------------------------------------------------------------------
-// Producer: one lane of warp 0.
+// Producer: one lane of warp 0 in every CTA.
 // ----------------------------------------------------------------------------
 template <class Cfg>
 __device__ __forceinline__ void run_producer(const SharedState& st, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                              const typename Cfg::Params& p) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
+  using P = Plan<Cfg>;
   const uint64_t polA = Cfg::policy_a();
   const uint64_t polB = Cfg::policy_b();
+  const bool leader = st.rank == 0;
   int stage = 0;
   uint32_t phase = 0;
   const int num_units = Cfg::num_units(p);
-  for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+  for (int u = st.unit_first; u < num_units; u += st.unit_stride) {
     const UnitInfo ui = Cfg::unit(p, u);
+    const int a_row = ui.m0 + static_cast<int>(st.rank) * BM;
     for (int j = 0; j < ui.ntiles; ++j) {
-      const int n0 = ui.n0 + j * Cfg::BN;
+      const int b_row = ui.n0 + j * Cfg::BN + static_cast<int>(st.rank) * P::B_ROWS;
       for (int kb = 0; kb < ui.nkb; ++kb) {
         if (!mbar_wait(&st.empty[stage], phase ^ 1u, st.abort, st.err, kDevTimeoutEmpty)) return;
-        const uint32_t sA = smem_u32(st.tiles + stage * Plan::STAGE_BYTES);
-        const uint32_t sB = sA + Plan::A_BYTES;
-        mbar_arrive_expect_tx(&st.full[stage], Plan::STAGE_BYTES);
+        const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
+        const uint32_t sB = sA + P::A_BYTES;
         const int kx = (ui.kb0 + kb) * BK;
-        if (!Cfg::A_MN) {
-          tma_load_2d(sA, tmA, &st.full[stage], kx, ui.m0, polA);
-        } else {
+        if (P::PAIR) {
+          if (leader) mbar_arrive_expect_tx(&st.full[stage], P::TX_BYTES);
+          const uint32_t bar = map_to_cta(smem_u32(&st.full[stage]), 0);
+          if (!Cfg::A_MN) {
+            tma_load_2d_pair(sA, tmA, bar, kx, a_row, polA);
+          } else {
 #pragma unroll
-          for (int i = 0; i < BM / 64; ++i) tma_load_2d(sA + i * 8192, tmA, &st.full[stage], ui.m0 + 64 * i, kx, polA);
-        }
-        if (!Cfg::B_MN) {
-          tma_load_2d(sB, tmB, &st.full[stage], kx, n0, polB);
-        } else {
+            for (int i = 0; i < BM / 64; ++i) tma_load_2d_pair(sA + i * 8192, tmA, bar, a_row + 64 * i, kx, polA);
+          }
+          if (!Cfg::B_MN) {
+            tma_load_2d_pair(sB, tmB, bar, kx, b_row, polB);
+          } else {
 #pragma unroll
-          for (int i = 0; i < Cfg::BN / 64; ++i) tma_load_2d(sB + i * 8192, tmB, &st.full[stage], n0 + 64 * i, kx, polB);
+            for (int i = 0; i < P::B_ROWS / 64; ++i)
+              tma_load_2d_pair(sB + i * 8192, tmB, bar, b_row + 64 * i, kx, polB);
+          }
+        } else {
+          mbar_arrive_expect_tx(&st.full[stage], P::TX_BYTES);
+          if (!Cfg::A_MN) {
+            tma_load_2d(sA, tmA, &st.full[stage], kx, a_row, polA);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(sA + i * 8192, tmA, &st.full[stage], a_row + 64 * i, kx, polA);
+          }
+          if (!Cfg::B_MN) {
+            tma_load_2d(sB, tmB, &st.full[stage], kx, b_row, polB);
+          } else {
+#pragma unroll
+            for (int i = 0; i < P::B_ROWS / 64; ++i)
+              tma_load_2d(sB + i * 8192, tmB, &st.full[stage], b_row + 64 * i, kx, polB);
+          }
         }
         if (++stage == Cfg::STAGES) {
           stage = 0;
@@ -111,7 +152,7 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
 }
 
 // ----------------------------------------------------------------------------
-// MMA issuer: one lane of warp 1.
+// MMA issuer: one lane of warp 1 (of the even CTA in pair mode).
 // ----------------------------------------------------------------------------
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
@@ -123,13 +164,13 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 template <class Cfg>
 __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
-  constexpr uint32_t idesc = make_idesc_bf16_f32(BM, Cfg::BN, Cfg::A_MN, Cfg::B_MN);
+  using P = Plan<Cfg>;
+  constexpr uint32_t idesc = make_idesc_bf16_f32(P::UM, Cfg::BN, Cfg::A_MN, Cfg::B_MN);
   int stage = 0;
   uint32_t phase = 0;
   uint32_t acc_i = 0;
   const int num_units = Cfg::num_units(p);
-  for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+  for (int u = st.unit_first; u < num_units; u += st.unit_stride) {
     const UnitInfo ui = Cfg::unit(p, u);
     for (int j = 0; j < ui.ntiles; ++j, ++acc_i) {
       const uint32_t buf = acc_i & 1u;
@@ -140,36 +181,50 @@ __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cf
       for (int kb = 0; kb < ui.nkb; ++kb) {
         if (!mbar_wait(&st.full[stage], phase, st.abort, st.err, kDevTimeoutFull)) return;
         tc_fence_after_sync();
-        const uint32_t sA = smem_u32(st.tiles + stage * Plan::STAGE_BYTES);
-        const uint32_t sB = sA + Plan::A_BYTES;
+        const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
+        const uint32_t sB = sA + P::A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          umma_bf16_f32(d_tmem, operand_desc<Cfg::A_MN>(sA, kk), operand_desc<Cfg::B_MN>(sB, kk), idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t ad = operand_desc<Cfg::A_MN>(sA, kk);
+          const uint64_t bd = operand_desc<Cfg::B_MN>(sB, kk);
+          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+          if (P::PAIR)
+            umma_bf16_f32_pair(d_tmem, ad, bd, idesc, acc);
+          else
+            umma_bf16_f32(d_tmem, ad, bd, idesc, acc);
         }
-        umma_commit(&st.empty[stage]);  // frees the stage once these MMAs have read it
+        // frees the stage (in both CTAs) once these MMAs have read it
+        if (P::PAIR)
+          umma_commit_pair_multicast(&st.empty[stage], 0x3);
+        else
+          umma_commit(&st.empty[stage]);
         if (++stage == Cfg::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      umma_commit(&st.tmem_full[buf]);  // accumulator ready for the epilogue
+      // accumulator ready for the epilogue (of both CTAs)
+      if (P::PAIR)
+        umma_commit_pair_multicast(&st.tmem_full[buf], 0x3);
+      else
+        umma_commit(&st.tmem_full[buf]);
     }
   }
 }
 
 // ----------------------------------------------------------------------------
-// Epilogue: warps 2..5.
+// Epilogue: warps 2..5 of every CTA.
 // ----------------------------------------------------------------------------
 template <class Cfg>
 __device__ __forceinline__ void run_epilogue(const SharedState& st, const typename Cfg::Params& p) {
+  using P = Plan<Cfg>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = warp & 3;          // TMEM lane group this warp may access
-  const int row = g * 32 + lane;   // accumulator row owned by this thread
+  const int g = warp & 3;                                          // TMEM lane group of this warp
+  const int row = static_cast<int>(st.rank) * BM + g * 32 + lane;  // accumulator row within the unit
   uint32_t acc_i = 0;
   const int num_units = Cfg::num_units(p);
-  for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+  for (int u = st.unit_first; u < num_units; u += st.unit_stride) {
     const UnitInfo ui = Cfg::unit(p, u);
     typename Cfg::RowState rs;
     Cfg::unit_begin(p, ui, u, row, rs);
@@ -179,9 +234,15 @@ __device__ __forceinline__ void run_epilogue(const SharedState& st, const typena
       if (!mbar_wait(&st.tmem_full[buf], acc_phase, st.abort, st.err, kDevTimeoutTmemFull)) return;
       tc_fence_after_sync();
       const uint32_t taddr = st.tmem_base + (static_cast<uint32_t>(g * 32) << 16) + buf * Cfg::BN;
-      Cfg::tile(p, ui, u, j, row, g, lane, taddr, rs);
+      Cfg::tile(p, ui, u, j, row, lane, taddr, rs);
       tc_fence_before_sync();
-      mbar_arrive(&st.tmem_empty[buf]);
+      __syncwarp();
+      if (lane == 0) {
+        if (P::PAIR)
+          mbar_arrive_cluster(map_to_cta(smem_u32(&st.tmem_empty[buf]), 0));
+        else
+          mbar_arrive(&st.tmem_empty[buf]);
+      }
     }
     Cfg::unit_end(p, ui, u, row, rs);
   }
@@ -191,14 +252,14 @@ template <class Cfg>
 __global__ void __launch_bounds__(kNumThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const typename Cfg::Params p) {
-  using Plan = SmemPlan<Cfg::BN, Cfg::STAGES, Cfg::EXTRA_SMEM>;
+  using P = Plan<Cfg>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   SharedState st;
   st.tiles = smem;
-  st.extra = smem + Plan::TILES_BYTES;
-  st.full = reinterpret_cast<uint64_t*>(smem + Plan::BAR_OFFSET);
+  st.extra = smem + P::TILES_BYTES;
+  st.full = reinterpret_cast<uint64_t*>(smem + P::BAR_OFFSET);
   st.empty = st.full + Cfg::STAGES;
   st.tmem_full = st.empty + Cfg::STAGES;
   st.tmem_empty = st.tmem_full + 2;
@@ -206,6 +267,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(st.drain + 1);
   st.abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   st.err = p.err;
+  st.rank = P::PAIR ? cluster_ctarank() : 0u;
+  st.unit_first = static_cast<int>(blockIdx.x) / P::NCTA;
+  st.unit_stride = static_cast<int>(gridDim.x) / P::NCTA;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -217,7 +281,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&st.tmem_full[b], 1);
-      mbar_init(&st.tmem_empty[b], kNumEpiThreads);
+      mbar_init(&st.tmem_empty[b], P::EPI_ARRIVALS);
     }
     mbar_init(st.drain, 1);
     *st.abort = 0;
@@ -227,23 +291,37 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  __syncwarp();  // the .aligned barriers and tcgen05 allocation below need converged warps
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish_alloc_permit();
+    if (P::PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_alloc_permit_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish_alloc_permit();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  // the peer's TMA loads and arrives target this CTA's barriers: both CTAs
+  // must have initialised them before either starts
+  if (P::PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after_sync();
   st.tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) run_producer<Cfg>(st, &tmA, &tmB, p);
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && st.rank == 0) {
       run_mma<Cfg>(st, p);
       // Every MMA this thread issued must have finished before TMEM is freed,
       // also when a role gave up early.
-      umma_commit(st.drain);
+      if (P::PAIR)
+        umma_commit_pair(st.drain);
+      else
+        umma_commit(st.drain);
       if (!mbar_wait_drain(st.drain, 0, 100000000ull)) atomicCAS(st.err, 0u, kDevTimeoutDrain);
     }
   } else {
@@ -251,9 +329,67 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 
   tc_fence_before_sync();
-  __syncthreads();
+  __syncwarp();  // lanes that skipped a role wait here for the one that ran it
+  // neither CTA of a pair may free TMEM or exit while the other can still
+  // touch its shared memory or TMEM
+  if (P::PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(st.tmem_base, kTmemCols);
+  if (warp == 1) {
+    if (P::PAIR)
+      tmem_dealloc_pair(st.tmem_base, kTmemCols);
+    else
+      tmem_dealloc(st.tmem_base, kTmemCols);
+  }
+}
+
+// Launch helper: pair configurations run as 2-CTA clusters.
+template <class Cfg>
+inline cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p, int grid,
+                               cudaStream_t s) {
+  using P = Plan<Cfg>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = P::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = P::NCTA;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Cfg>, a, b, p);
+}
+
+// One-time set-up per kernel: shared-memory opt-in and the number of clusters
+// (CTAs in single mode) that can be resident at once, which bounds the grid of
+// the persistent kernel so that no CTA waits for a second wave.
+template <class Cfg>
+inline cudaError_t setup_gemm(int* resident_groups) {
+  using P = Plan<Cfg>;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P::NCTA, 1, 1);
+  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = P::TOTAL;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = P::NCTA;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int groups = 0;
+  e = cudaOccupancyMaxActiveClusters(&groups, tc_gemm_kernel<Cfg>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (groups < 1) return cudaErrorInvalidConfiguration;
+  *resident_groups = groups;
+  return cudaSuccess;
 }
 
 }  // namespace llp

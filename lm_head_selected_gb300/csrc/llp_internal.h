@@ -17,7 +17,19 @@ constexpr int kTileK = 64;            // K elements per pipeline stage
 constexpr int kTilesPerSplit = 2;     // forward vocab split = 512 columns
 constexpr int kSplitWidth = kTileN * kTilesPerSplit;
 constexpr int kKSegment = 32768;      // fixed K segment of the gradient GEMMs
-constexpr int kGroupM = 64;           // L2 raster group (M tiles); scheduling only
+constexpr bool kPairMMA = true;       // 2-CTA (cta_group::2) tiles: 256 rows per unit
+constexpr int kUnitM = kPairMMA ? 2 * kTileM : kTileM;  // unit rows (M) per tile
+constexpr int kBRows = kPairMMA ? kTileN / 2 : kTileN;  // rows of a K-major B tile each CTA loads
+constexpr int kGroupM = 32;           // L2 raster group (unit M tiles); scheduling only
+
+// Resident work groups (CTA pairs, or CTAs in single mode) per GEMM kernel,
+// found once per device; the persistent grids never exceed them.
+struct LaunchCaps {
+  int fwd_groups[2];  // [has_bias]
+  int dz_groups[2];   // [has_bias]
+  int gh_groups;
+  int gw_groups;
+};
 
 struct FwdParams {
   int N, D, V;
@@ -56,19 +68,20 @@ struct GradGemmParams {
   unsigned int* err;
 };
 
-// Launchers (return the launch error, never synchronise).
-cudaError_t fwd_setup();
-cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p, int grid,
-                                cudaStream_t s);
+// Launchers (return the launch error, never synchronise).  `units` is the
+// number of work units; the grid is min(units, resident groups) groups.
+cudaError_t fwd_setup(LaunchCaps* caps);
+cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,
+                                long long units, const LaunchCaps& caps, cudaStream_t s);
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s);
 
-cudaError_t bwd_setup();
-cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, int grid,
-                           cudaStream_t s);
+cudaError_t bwd_setup(LaunchCaps* caps);
+cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, long long units,
+                           const LaunchCaps& caps, cudaStream_t s);
 cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const GradGemmParams& p,
-                               int grid, cudaStream_t s);
+                               long long units, const LaunchCaps& caps, cudaStream_t s);
 cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const GradGemmParams& p,
-                               int grid, cudaStream_t s);
+                               long long units, const LaunchCaps& caps, cudaStream_t s);
 cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s);
 cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s);
 
