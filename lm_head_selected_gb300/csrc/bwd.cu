@@ -62,7 +62,7 @@ struct DzCfg {
   static constexpr bool B_MN = false;
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int STAGES = PAIR ? kPairStages : 4;
   static constexpr int EXTRA_SMEM = 0;
   static constexpr int UM = kUnitM;
   using Params = DzParams;
@@ -181,7 +181,7 @@ struct GradCfg {
   static constexpr bool B_MN = B_MN_;
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int STAGES = PAIR ? kPairStages : 4;
   static constexpr int EXTRA_SMEM = 0;
   static constexpr int UM = kUnitM;
   using Params = GradGemmParams;

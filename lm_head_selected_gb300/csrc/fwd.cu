@@ -34,7 +34,7 @@ struct FwdCfg {
   static constexpr bool B_MN = false;
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int STAGES = PAIR ? kPairStages : 4;
   static constexpr int EXTRA_SMEM = 0;
   static constexpr int TPS = kTilesPerSplit;
   static constexpr int UM = kUnitM;

@@ -20,7 +20,15 @@ constexpr int kKSegment = 32768;      // fixed K segment of the gradient GEMMs
 constexpr bool kPairMMA = true;       // 2-CTA (cta_group::2) tiles: 256 rows per unit
 constexpr int kUnitM = kPairMMA ? 2 * kTileM : kTileM;  // unit rows (M) per tile
 constexpr int kBRows = kPairMMA ? kTileN / 2 : kTileN;  // rows of a K-major B tile each CTA loads
-constexpr int kGroupM = 32;           // L2 raster group (unit M tiles); scheduling only
+// Compile-time tuning knobs (defaults are the tuned values).
+#ifndef LLP_GROUP_M
+#define LLP_GROUP_M 32     // L2 raster group in unit M tiles (256 rows); scheduling only
+#endif
+constexpr int kGroupM = LLP_GROUP_M;
+#ifndef LLP_PAIR_STAGES
+#define LLP_PAIR_STAGES 6  // shared-memory pipeline stages in pair mode (32 KB each)
+#endif
+constexpr int kPairStages = LLP_PAIR_STAGES;
 
 // Resident work groups (CTA pairs, or CTAs in single mode) per GEMM kernel,
 // found once per device; the persistent grids never exceed them.
