@@ -43,6 +43,10 @@ WORKLOADS = {
     # smaller token count of the same head, for profiler captures (weight still > L2)
     "rl_head_small": (2048, 2688, 131072,
                       "same head and distributions with N=2048 (for profiler captures)"),
+    # batch 2 x seq 16 on the same head: the weight stream bounds every kernel (HBM roofline)
+    "nemotron_n32": (32, 2688, 131072,
+                     "Nemotron-3-Nano LM head, N=32 (2x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
+                     "uniform targets, grad_logp=1"),
 }
 # The pages' number for this metric and workload: strict fused fwd+bwd, 16384 tokens,
 # D=2688, V=131072, 351.2 ms on an H100 PCIe ("Feat/nemotron h lm head logprob cuda",
@@ -158,8 +162,10 @@ def cpu_cores_used() -> int:
 def oracle_sample_seconds(inp, rows: int) -> float:
     """Time the FP64 oracle's forward + backward on the first `rows` tokens."""
     import oracle
-    sub = inp.rows(list(range(rows)))
-    a = (sub.hidden.double().numpy(), sub.weight.double().numpy(), None, sub.targets.numpy(), None, -100)
+    sub = inp.rows(list(range(min(rows, inp.N))))
+    a = (sub.hidden.double().numpy(), sub.weight.double().numpy(),
+         None if sub.bias is None else sub.bias.double().numpy(), sub.targets.numpy(),
+         None if sub.temperature is None else sub.temperature.double().numpy(), sub.ignore_index)
     g = sub.grad_logp.double().numpy()
     t0 = time.perf_counter()
     oracle.forward(*a)
@@ -170,8 +176,41 @@ def oracle_sample_seconds(inp, rows: int) -> float:
 def make_workload(name):
     import workloads
     N, D, V, desc = WORKLOADS[name]
-    inp = workloads.rl_scoring(N=N, D=D, V=V, seed=1002, grad_std=1.0)
+    if name == "nemotron_n32":
+        inp = workloads.nemotron_head(N=N, seed=1001)
+    else:
+        inp = workloads.rl_scoring(N=N, D=D, V=V, seed=1002, grad_std=1.0)
     return inp, desc
+
+
+def kernel_model(name, N, D, V, has_bias, has_tau):
+    """Algorithmic (flop, byte) count of one launch of each kernel of the path:
+    every operand read once, every result written once."""
+    S = -(-V // 512)
+    Vp = -(-V // 64) * 64
+    nseg_v = -(-V // 32768)
+    nseg_n = -(-N // 32768)
+    W = 2.0 * V * D
+    H = 2.0 * N * D
+    row_in = 8.0 * N + (4.0 * N if has_tau else 0.0) + (4.0 * V if has_bias else 0.0)
+    gemm = 2.0 * N * V * D
+    if name == "fwd_partials":
+        return gemm, W + H + row_in + 8.0 * S * N + 4.0 * N
+    if name == "fwd_merge":
+        return 0.0, 8.0 * S * N + 4.0 * N + 8.0 * N + 8.0 * N
+    if name == "dlogits":
+        return gemm, W + H + row_in + 8.0 * N + 2.0 * N * Vp + (4.0 * V * (-(-N // 32)) if has_bias else 0.0)
+    if name == "grad_hidden":
+        return gemm, 2.0 * N * V + W + (4.0 * nseg_v * N * D if nseg_v > 1 else 2.0 * N * D)
+    if name == "segment_sum_hidden":
+        return 0.0, 4.0 * nseg_v * N * D + 2.0 * N * D
+    if name == "grad_weight":
+        return gemm, 2.0 * N * V + H + (4.0 * nseg_n * V * D if nseg_n > 1 else W)
+    if name == "segment_sum_weight":
+        return 0.0, 4.0 * nseg_n * V * D + W
+    if name == "bias_sum":
+        return 0.0, 4.0 * V * (-(-N // 32)) + 4.0 * V
+    return 0.0, 0.0
 
 
 def run_reference(args):
@@ -179,7 +218,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     inp, desc = make_workload(args.workload)
-    rows = args.reference_rows
+    rows = min(args.reference_rows, inp.N)
     for _ in range(args.warmup):
         oracle_sample_seconds(inp, rows)
     times = [oracle_sample_seconds(inp, rows) for _ in range(args.steps)]
@@ -219,14 +258,16 @@ def run_ours(args):
     w = inp.weight.to(dev)
     t = inp.targets.to(dev)
     g = inp.grad_logp.to(dev)
+    b = None if inp.bias is None else inp.bias.to(dev)
+    tau = None if inp.temperature is None else inp.temperature.to(dev)
     ws_f = torch.empty(llp.fwd_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(llp.bwd_workspace_bytes(N, D, V, False), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(llp.bwd_workspace_bytes(N, D, V, b is not None), dtype=torch.uint8, device=dev)
     logp = torch.empty(N, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
 
     def step():
-        llp.linear_logp_fwd(h, w, t, workspace=ws_f, out=(logp, lse))
-        return llp.linear_logp_bwd(g, lse, h, w, t, workspace=ws_b)
+        llp.linear_logp_fwd(h, w, t, b, tau, workspace=ws_f, out=(logp, lse))
+        return llp.linear_logp_bwd(g, lse, h, w, t, b, tau, workspace=ws_b)
 
     def barrier():
         torch.cuda.synchronize()
@@ -268,20 +309,24 @@ def run_ours(args):
         d = per.setdefault(name, {"launches": 0, "ms_total": 0.0})
         d["launches"] += 1
         d["ms_total"] += ms
+    peaks = load_peaks()
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
     kernels = {}
     for name, d in per.items():
         avg = d["ms_total"] / d["launches"]
+        fl, by = kernel_model(name, N, D, V, b is not None, tau is not None)
         kernels[name] = {"launches_per_step": d["launches"] / args.steps, "ms_per_launch": avg,
-                         "share": d["ms_total"] / max(sum(x["ms_total"] for x in per.values()), 1e-9)}
-        if name in GEMM_KERNELS:
-            kernels[name]["tflops"] = 2.0 * N * V * D / (avg * 1e-3) / 1e12
+                         "share": d["ms_total"] / max(sum(x["ms_total"] for x in per.values()), 1e-9),
+                         "algorithmic_gb": by / 1e9, "gbs": by / (avg * 1e-3) / 1e9,
+                         "bound": "tensor" if fl > ridge * by else "hbm"}
+        if fl > 0:
+            kernels[name]["tflops"] = fl / (avg * 1e-3) / 1e12
 
-    peaks = load_peaks()
     flops_counted = 6.0 * N * V * D
     step_tflops = flops_counted / (ms_step * 1e-3) / 1e12
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches_per_step"])
     dk = kernels[dom]
-    if dom in GEMM_KERNELS:
+    if dk["bound"] == "tensor":
         achieved = dk["tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops_sustained"], "kernel": dom,
@@ -289,8 +334,12 @@ def run_ours(args):
                 "peak_kind": f"bf16 sustained ({peaks['source']}); kernel timed inside back-to-back steps",
                 "algorithmic_per_launch": f"2*N*V*D = {2.0 * N * V * D:.4e} flop"}
     else:
-        roof = {"bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": None,
-                "kernel": dom}
+        achieved = dk["gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "kernel": dom,
+                "peak_kind": f"HBM copy bandwidth ({peaks['source']})",
+                "algorithmic_per_launch": f"{dk['algorithmic_gb'] * 1e9:.4e} bytes (every operand read once, "
+                                          f"every result written once)"}
     roof["traffic"] = None
     if NCU_TRAFFIC and NCU_TRAFFIC.get("kernel") == dom and NCU_TRAFFIC.get("sources_sha") == sources_sha():
         roof["traffic"] = NCU_TRAFFIC["bytes_per_launch"]
@@ -301,7 +350,7 @@ def run_ours(args):
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(args.steps):
-        llp.linear_logp_fwd(h, w, t, workspace=ws_f, out=(logp, lse))
+        llp.linear_logp_fwd(h, w, t, b, tau, workspace=ws_f, out=(logp, lse))
     f1.record(stream)
     barrier()
     fwd_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.steps
@@ -311,15 +360,20 @@ def run_ours(args):
     h_host = inp.hidden.pin_memory()
     t_host = inp.targets.pin_memory()
     g_host = inp.grad_logp.pin_memory()
+    tau_host = None if inp.temperature is None else inp.temperature.pin_memory()
     out_host = torch.empty(N, dtype=torch.float32).pin_memory()
     w_param = w.detach().clone().requires_grad_(True)
+    b_param = None if b is None else b.detach().clone().requires_grad_(True)
 
     def e2e_step():
         hd = h_host.to(dev, non_blocking=True).requires_grad_(True)
         td = t_host.to(dev, non_blocking=True)
         gd = g_host.to(dev, non_blocking=True)
+        taud = None if tau_host is None else tau_host.to(dev, non_blocking=True)
         w_param.grad = None
-        lp = llp.linear_logp(hd, w_param, td)
+        if b_param is not None:
+            b_param.grad = None
+        lp = llp.linear_logp(hd, w_param, td, b_param, taud)
         lp.backward(gd)
         out_host.copy_(lp.detach(), non_blocking=True)
 
@@ -334,12 +388,12 @@ def run_ours(args):
     t1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
-    h2d = h_host.numel() * 2 + t_host.numel() * 8 + g_host.numel() * 4
+    h2d = h_host.numel() * 2 + t_host.numel() * 8 + g_host.numel() * 4 + (0 if tau_host is None else 4 * N)
     d2h = out_host.numel() * 4
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rows = args.cpu_rows
+        rows = min(args.cpu_rows, N)
         secs = oracle_sample_seconds(inp, rows)
         cpu = {"value": rows / secs, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
                "sample": f"first {rows} of {N} tokens, full D={D} and V={V}, FP64 forward+backward, "
@@ -351,7 +405,7 @@ def run_ours(args):
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": value / PAGES_TOKENS_PER_S, "vs_baseline_context": PAGES_CONTEXT,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "N": N, "D": D, "V": V, "bias": False, "temperature": False,
+            "config": {"workload": args.workload, "N": N, "D": D, "V": V, "bias": b is not None, "temperature": tau is not None,
                        "description": desc, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (weight 704.6 MB > 129 MB), no flush"},
             "tensor_peak_frac": step_tflops / peaks["bf16_tflops_sustained"],
@@ -377,6 +431,78 @@ def run_ours(args):
     return 0
 
 
+def run_fused(args):
+    """Logits-input fused log-prob: forward (row statistics + target gather) and
+    backward (grad_logits from the saved statistics) over bf16 logits [N, V];
+    bound by HBM bandwidth (forward reads every logit once; backward reads every
+    logit and writes every gradient once)."""
+    import torch
+
+    from lm_head_selected_gb300 import build
+    build.build()
+    import lm_head_selected_gb300 as llp
+
+    N, V = args.fused_n, args.fused_v
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(1005)
+    z = (torch.randn(N, V, generator=g) * 3.0).to(torch.bfloat16).to(dev)
+    t = torch.randint(0, V, (N,), generator=g).to(dev)
+    gl = torch.randn(N, generator=g).to(dev)
+    from lm_head_selected_gb300 import _lib
+    ws = torch.empty(_lib.load().fused_logp_workspace_bytes(N, V), dtype=torch.uint8, device=dev)
+    grad = torch.empty_like(z)
+
+    def fwd():
+        return llp.fused_logp_fwd(z, t, workspace=ws)
+
+    _, m, ls = fwd()
+
+    def bwd():
+        llp.fused_logp_bwd(gl, m, ls, z, t, out=grad)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    f_ms = timed(fwd)
+    b_ms = timed(bwd)
+    clk = clocks.stop()
+    peaks = load_peaks()
+    S = -(-V // 16384)
+    f_bytes = 2.0 * N * V + 8.0 * N * S + 8.0 * N + 12.0 * N
+    b_bytes = 2.0 * N * V * 2 + 8.0 * N + 12.0 * N
+    f_gbs = f_bytes / (f_ms * 1e-3) / 1e9
+    b_gbs = b_bytes / (b_ms * 1e-3) / 1e9
+    dom_name, dom_gbs, dom_bytes = ("fused_grad", b_gbs, b_bytes) if b_ms >= f_ms else ("fused_split", f_gbs, f_bytes)
+    line = {
+        "metric": "logits-input fused logp fwd+bwd tokens/s (HBM-bound)", "value": N / ((f_ms + b_ms) * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": f_ms + b_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"fused_logp N={N} V={V} bf16 logits", "N": N, "V": V,
+                   "l2": f"inputs larger than L2 ({2.0 * N * V / 1e9:.2f} GB of logits)"},
+        "fwd": {"ms": f_ms, "gbs": f_gbs, "frac_of_hbm": f_gbs / peaks["hbm_gbs"]},
+        "bwd": {"ms": b_ms, "gbs": b_gbs, "frac_of_hbm": b_gbs / peaks["hbm_gbs"]},
+        "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": dom_gbs / peaks["hbm_gbs"], "kernel": dom_name, "traffic": None,
+                     "algorithmic_per_launch": f"{dom_bytes:.4e} bytes"},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -387,7 +513,13 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the timed oracle sample")
     ap.add_argument("--reference-rows", type=int, default=64, help="token rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=("linear_logp", "fused_logp"), default="linear_logp",
+                    help="linear_logp: the fused LM-head path (default); fused_logp: the logits-input op")
+    ap.add_argument("--fused-n", type=int, default=16384)
+    ap.add_argument("--fused-v", type=int, default=131072)
     args = ap.parse_args(argv)
+    if args.op == "fused_logp":
+        return run_fused(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -145,6 +145,33 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
                     int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Row-subset (indexed) variants ("recursive deterministic LogP autograd on
+ * B200", What: indexed semantics; "add backward support for fused logp CUDA
+ * kernels", Implementation details: zero gradients for rows omitted by indexed
+ * variants).  `indices` [K] int64 (device) names the token rows to compute;
+ * duplicates count once, entries outside [0, N) are ignored.
+ *   linear_logp_fwd_indexed writes out_logp[i] / out_lse[i] for each selected
+ *     row i (bitwise the values linear_logp_fwd gives that row) and leaves every
+ *     other entry of out_logp / out_lse untouched.
+ *   linear_logp_bwd_indexed returns the gradients of sum over selected rows i of
+ *     grad_logp[i] * logp[i]: grad_hidden is written for all N rows (zero for
+ *     rows not selected); grad_weight / grad_bias sum over the selected rows.
+ * Same arguments, checks and conventions as the plain calls otherwise; the
+ * workspace is sized by the *_indexed_workspace_bytes queries (K = len(indices)).
+ */
+size_t linear_logp_fwd_indexed_workspace_bytes(int64_t N, int64_t D, int64_t V, int64_t K);
+size_t linear_logp_bwd_indexed_workspace_bytes(int64_t N, int64_t D, int64_t V, int64_t K, int has_bias);
+int linear_logp_fwd_indexed(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                            const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                            const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
+int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                            const float* bias, const int64_t* targets, const float* temperature, int64_t N,
+                            int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
+                            void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* linear_logp_status_string(int status);
 
@@ -165,6 +192,16 @@ const char* linear_logp_status_string(int status);
 int linear_logp_profile_start(int capacity);
 int linear_logp_profile_stop(int* kernel_ids, float* ms, int capacity);
 const char* linear_logp_kernel_name(int kernel_id);
+
+/* Diagnostic: checks that a bounded wait in device code gives up and reports
+ * instead of hanging.  Enqueues on `stream` one single-thread kernel that waits
+ * on a barrier nothing will ever complete, with a limit of `limit_ns`
+ * nanoseconds (1 .. 10^9); when the limit passes the kernel records
+ * LINEAR_LOGP_DEVICE_SELFTEST_CODE in the status word and returns normally, so
+ * the context stays usable.  Read the outcome with linear_logp_device_status.
+ * Returns LLP_OK, LLP_ERR_BAD_SHAPE for a limit out of range, or an error. */
+#define LINEAR_LOGP_DEVICE_SELFTEST_CODE 6u
+int linear_logp_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
 /* Synchronises `stream`, then reads and clears the current device's kernel
  * status word.  Returns LLP_OK if no kernel gave up on a wait since the last

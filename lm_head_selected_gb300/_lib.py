@@ -31,7 +31,19 @@ EXPORTED = (
     "linear_logp_profile_stop",
     "linear_logp_kernel_name",
     "linear_logp_fwd_noalloc",
+    "linear_logp_selftest_wait_timeout",
+    "linear_logp_fwd_indexed_workspace_bytes",
+    "linear_logp_bwd_indexed_workspace_bytes",
+    "linear_logp_fwd_indexed",
+    "linear_logp_bwd_indexed",
 )
+# include/fused_logp.h (logits-input op, same library)
+EXPORTED_FUSED = (
+    "fused_logp_workspace_bytes",
+    "fused_logp_fwd",
+    "fused_logp_bwd",
+)
+DEVICE_SELFTEST_CODE = 6
 LLP_ERR_SCRATCH_LIMIT = -8
 
 _lock = threading.Lock()
@@ -88,6 +100,24 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_kernel_name.restype = ctypes.c_char_p
         lib.linear_logp_fwd_noalloc.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _p, _p]
         lib.linear_logp_fwd_noalloc.restype = ctypes.c_int
+        lib.linear_logp_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _p]
+        lib.linear_logp_selftest_wait_timeout.restype = ctypes.c_int
+        lib.linear_logp_fwd_indexed_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
+        lib.linear_logp_fwd_indexed_workspace_bytes.restype = _size
+        lib.linear_logp_bwd_indexed_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int]
+        lib.linear_logp_bwd_indexed_workspace_bytes.restype = _size
+        lib.linear_logp_fwd_indexed.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _i64, _p, _p, _p,
+                                                _size, _p]
+        lib.linear_logp_fwd_indexed.restype = ctypes.c_int
+        lib.linear_logp_bwd_indexed.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _i64, _p,
+                                                _p, _p, _p, _size, _p]
+        lib.linear_logp_bwd_indexed.restype = ctypes.c_int
+        lib.fused_logp_workspace_bytes.argtypes = [_i64, _i64]
+        lib.fused_logp_workspace_bytes.restype = _size
+        lib.fused_logp_fwd.argtypes = [_p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _p, _p, _p, _size, _p]
+        lib.fused_logp_fwd.restype = ctypes.c_int
+        lib.fused_logp_bwd.argtypes = [_p, _p, _p, _p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _p]
+        lib.fused_logp_bwd.restype = ctypes.c_int
         _lib = lib
         return lib
 

@@ -6,8 +6,10 @@
 #include <mutex>
 #include <vector>
 
+#include "fused_logp.h"
 #include "linear_logp.h"
 #include "llp_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -168,6 +170,25 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
 }
 
+// Output map of fp32 segment partials [nseg][rows][cols], box {32, 32, 1}:
+// a store clips at `rows` inside each segment.
+int make_map_part(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t nseg) {
+  cuuint64_t dims[3] = {cols, rows, nseg};
+  cuuint64_t strides[2] = {cols * 4, rows * cols * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
+}
+
+// Output map of a gradient [rows][D] (bf16) or of its segment partials.
+int make_map_grad_out(CUtensorMap* m, const llp::GradGemmParams& p) {
+  if (p.nseg == 1) return make_map(m, p.out, p.D, p.rows, static_cast<uint64_t>(p.D) * 2, 64, 32);
+  return make_map_part(m, p.part, p.D, p.rows, p.nseg);
+}
+
 // ----------------------------------------------------------------------------
 // Optional launch recorder (see linear_logp_profile_start in the header).
 // ----------------------------------------------------------------------------
@@ -211,6 +232,149 @@ void rec_mark(cudaStream_t s, int id) {
   g_rec.ids[g_rec.used] = id;
   ++g_rec.used;
 }
+
+// Forward launch sequence on validated arguments (N > 0, workspace sized by fwd_layout).
+int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+             const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index, float* out_logp,
+             float* out_lse, uint8_t* ws, cudaStream_t s) {
+  const FwdLayout L = fwd_layout(N, V);
+  CUtensorMap tm_h, tm_w;
+  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
+  llp::FwdParams p;
+  p.N = static_cast<int>(N);
+  p.D = static_cast<int>(D);
+  p.V = static_cast<int>(V);
+  p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+  p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
+  p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
+  p.group_m = llp::kGroupM;
+  p.bias = bias;
+  p.targets = reinterpret_cast<const long long*>(targets);
+  p.temperature = temperature;
+  p.ignore_index = ignore_index;
+  p.part_m = reinterpret_cast<float*>(ws + L.part_m);
+  p.part_s = reinterpret_cast<float*>(ws + L.part_s);
+  p.zt = reinterpret_cast<float*>(ws + L.zt);
+  p.err = dev->status_ptr;
+  const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
+  rec_mark(s, -1);
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
+  rec_mark(s, kKFwdPartials);
+  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+  rec_mark(s, kKFwdMerge);
+  return LLP_OK;
+}
+
+// Backward launch sequence on validated arguments (N > 0, workspace sized by bwd_layout).
+int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+             const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V,
+             int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias, uint8_t* ws,
+             cudaStream_t s) {
+  const bool want_gb = grad_bias != nullptr;
+  const BwdLayout L = bwd_layout(N, D, V, bias != nullptr, grad_hidden != nullptr, grad_weight != nullptr);
+  const int64_t V_pad = static_cast<int64_t>(round_up(static_cast<size_t>(V), 64));
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + L.dz);
+
+  // B1: dlogits (+ grad_bias partials)
+  {
+    CUtensorMap tm_h, tm_w;
+    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
+    llp::DzParams p;
+    p.N = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.V = static_cast<int>(V);
+    p.V_pad = static_cast<int>(V_pad);
+    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+    p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
+    p.group_m = llp::kGroupM;
+    p.bias = bias;
+    p.targets = reinterpret_cast<const long long*>(targets);
+    p.temperature = temperature;
+    p.ignore_index = ignore_index;
+    p.grad_logp = grad_logp;
+    p.lse = saved_lse;
+    p.dz = dz;
+    p.gb_part = want_gb ? reinterpret_cast<float*>(ws + L.gb_part) : nullptr;
+    p.err = dev->status_ptr;
+    const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
+    rec_mark(s, -1);
+    CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
+    if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32) != LLP_OK) return LLP_ERR_CUDA;
+    if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
+    rec_mark(s, kKDlogits);
+  }
+
+  // B2: grad_hidden = dz . W over fixed vocab segments
+  if (grad_hidden != nullptr) {
+    CUtensorMap tm_dz, tm_w_mn;
+    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    llp::GradGemmParams p;
+    p.rows = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.K = static_cast<int>(V);
+    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
+    p.nseg = static_cast<int>(cdiv(V, llp::kKSegment));
+    p.kseg_blocks = llp::kKSegment / llp::kTileK;
+    p.out = static_cast<__nv_bfloat16*>(grad_hidden);
+    p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
+    p.err = dev->status_ptr;
+    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
+    CUtensorMap tm_out;
+    if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;
+    if (llp::launch_grad_hidden(tm_dz, tm_w_mn, tm_out, p, units, dev->caps, s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    rec_mark(s, kKGradHidden);
+    if (p.nseg > 1) {
+      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s) != cudaSuccess)
+        return LLP_ERR_CUDA;
+      rec_mark(s, kKSegSumHidden);
+    }
+  }
+
+  // B3: grad_weight = dz^T . h over fixed token segments
+  if (grad_weight != nullptr) {
+    CUtensorMap tm_dz_mn, tm_h_mn;
+    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    llp::GradGemmParams p;
+    p.rows = static_cast<int>(V);
+    p.D = static_cast<int>(D);
+    p.K = static_cast<int>(N);
+    p.num_m = static_cast<int>(cdiv(V, llp::kUnitM));
+    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
+    p.nseg = static_cast<int>(cdiv(N, llp::kKSegment));
+    p.kseg_blocks = llp::kKSegment / llp::kTileK;
+    p.out = static_cast<__nv_bfloat16*>(grad_weight);
+    p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
+    p.err = dev->status_ptr;
+    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
+    CUtensorMap tm_out;
+    if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;
+    if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, tm_out, p, units, dev->caps, s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    rec_mark(s, kKGradWeight);
+    if (p.nseg > 1) {
+      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s) != cudaSuccess)
+        return LLP_ERR_CUDA;
+      rec_mark(s, kKSegSumWeight);
+    }
+  }
+
+  // B4: grad_bias
+  if (want_gb) {
+    const int nblocks = static_cast<int>(cdiv(N, llp::kUnitM) * (llp::kUnitM / 32));
+    if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
+                             s) != cudaSuccess)
+      return LLP_ERR_CUDA;
+    rec_mark(s, kKBiasSum);
+  }
+  return LLP_OK;
+}
+
 
 }  // namespace
 
@@ -260,37 +424,8 @@ int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, c
   DeviceInit* dev = nullptr;
   if ((st = init_device(&dev)) != LLP_OK) return st;
   if ((st = load_encode_fn()) != LLP_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  CUtensorMap tm_h, tm_w;
-  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  llp::FwdParams p;
-  p.N = static_cast<int>(N);
-  p.D = static_cast<int>(D);
-  p.V = static_cast<int>(V);
-  p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
-  p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
-  p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
-  p.group_m = llp::kGroupM;
-  p.bias = bias;
-  p.targets = reinterpret_cast<const long long*>(targets);
-  p.temperature = temperature;
-  p.ignore_index = ignore_index;
-  p.part_m = reinterpret_cast<float*>(ws + L.part_m);
-  p.part_s = reinterpret_cast<float*>(ws + L.part_s);
-  p.zt = reinterpret_cast<float*>(ws + L.zt);
-  p.err = dev->status_ptr;
-
-  const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
-  rec_mark(s, -1);
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
-  rec_mark(s, kKFwdPartials);
-  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
-  rec_mark(s, kKFwdMerge);
-  return LLP_OK;
+  return fwd_core(dev, hidden, weight, bias, targets, temperature, N, D, V, ignore_index, out_logp, out_lse,
+                  static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
@@ -321,7 +456,6 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
   if (st != LLP_OK) return st;
   if (grad_logp == nullptr || saved_lse == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(grad_logp, 4) || !aligned(saved_lse, 4)) return LLP_ERR_MISALIGNED;
-  const bool want_gb = grad_bias != nullptr;
   const BwdLayout L = bwd_layout(N, D, V, bias != nullptr, grad_hidden != nullptr, grad_weight != nullptr);
   if (workspace == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
@@ -329,102 +463,232 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
 
   if ((st = init_device(&dev)) != LLP_OK) return st;
   if ((st = load_encode_fn()) != LLP_OK) return st;
+  return bwd_core(dev, grad_logp, saved_lse, hidden, weight, bias, targets, temperature, N, D, V, ignore_index,
+                  grad_hidden, grad_weight, grad_bias, static_cast<uint8_t*>(workspace), s);
+}
 
+// ----------------------------------------------------------------------------
+// Row-subset (indexed) variants: select -> gather a compact problem of
+// Kc = min(K, N) rows (padding slots carry an ignored target) -> the plain
+// launch sequence on it -> scatter back.  Every launch size is known on the host.
+// ----------------------------------------------------------------------------
+struct IdxLayout {
+  size_t sel, c_hidden, c_targets, c_temp, c_a, c_b, c_gh, inner, total;
+  int64_t Kc;
+};
+
+static IdxLayout idx_layout(int64_t N, int64_t D, int64_t V, int64_t K, bool bwd, bool bias) {
+  IdxLayout L;
+  L.Kc = K < N ? K : N;
+  const size_t Kc = static_cast<size_t>(L.Kc);
+  Carver c;
+  L.sel = c.take(llp::select_workspace_bytes(N, K));
+  L.c_hidden = c.take(Kc * D * 2);
+  L.c_targets = c.take(Kc * 8);
+  L.c_temp = c.take(Kc * 4);
+  L.c_a = c.take(Kc * 4);  // forward: compact logp; backward: compact grad_logp
+  L.c_b = c.take(Kc * 4);  // compact lse
+  L.c_gh = bwd ? c.take(Kc * D * 2) : 0;
+  L.inner = c.take(L.Kc > 0 ? (bwd ? bwd_layout(L.Kc, D, V, bias, true, true).total : fwd_layout(L.Kc, V).total) : 0);
+  L.total = c.off;
+  return L;
+}
+
+size_t linear_logp_fwd_indexed_workspace_bytes(int64_t N, int64_t D, int64_t V, int64_t K) {
+  if (N <= 0 || K <= 0 || check_shapes(N, D, V) != LLP_OK) return 0;
+  return idx_layout(N, D, V, K, false, false).total;
+}
+
+size_t linear_logp_bwd_indexed_workspace_bytes(int64_t N, int64_t D, int64_t V, int64_t K, int has_bias) {
+  if (N <= 0 || K <= 0 || check_shapes(N, D, V) != LLP_OK) return 0;
+  return idx_layout(N, D, V, K, true, has_bias != 0).total;
+}
+
+int linear_logp_fwd_indexed(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                            const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                            const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  int st = check_shapes(N, D, V);
+  if (st != LLP_OK) return st;
+  if (K < 0 || K > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (N == 0 || K == 0) return LLP_OK;  // nothing selected: outputs untouched
+  if (indices == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(indices, 8)) return LLP_ERR_MISALIGNED;
+  st = check_inputs(hidden, weight, bias, targets, temperature, N, D, V);
+  if (st != LLP_OK) return st;
+  if (out_logp == nullptr || out_lse == nullptr || workspace == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(out_logp, 4) || !aligned(out_lse, 4) || !aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
+  const IdxLayout L = idx_layout(N, D, V, K, false, false);
+  if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int64_t V_pad = static_cast<int64_t>(round_up(static_cast<size_t>(V), 64));
-  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + L.dz);
+  llp::RowSelection sel;
+  if (llp::build_row_selection(reinterpret_cast<const long long*>(indices), K, static_cast<int>(N), ws + L.sel, &sel,
+                               s) != cudaSuccess)
+    return LLP_ERR_CUDA;
+  auto* c_hidden = reinterpret_cast<__nv_bfloat16*>(ws + L.c_hidden);
+  auto* c_targets = reinterpret_cast<long long*>(ws + L.c_targets);
+  float* c_temp = temperature ? reinterpret_cast<float*>(ws + L.c_temp) : nullptr;
+  if (llp::gather_selected_rows(sel, static_cast<int>(D), static_cast<const __nv_bfloat16*>(hidden),
+                                reinterpret_cast<const long long*>(targets), temperature, nullptr, nullptr,
+                                ignore_index, c_hidden, c_targets, c_temp, nullptr, nullptr, s) != cudaSuccess)
+    return LLP_ERR_CUDA;
+  float* c_logp = reinterpret_cast<float*>(ws + L.c_a);
+  float* c_lse = reinterpret_cast<float*>(ws + L.c_b);
+  st = fwd_core(dev, c_hidden, weight, bias, reinterpret_cast<const int64_t*>(c_targets), c_temp, L.Kc, D, V,
+                ignore_index, c_logp, c_lse, ws + L.inner, s);
+  if (st != LLP_OK) return st;
+  return llp::scatter_selected_outputs(sel, c_logp, c_lse, out_logp, out_lse, s) == cudaSuccess ? LLP_OK
+                                                                                                : LLP_ERR_CUDA;
+}
 
-  // B1: dlogits (+ grad_bias partials)
-  {
-    CUtensorMap tm_h, tm_w;
-    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
-    llp::DzParams p;
-    p.N = static_cast<int>(N);
-    p.D = static_cast<int>(D);
-    p.V = static_cast<int>(V);
-    p.V_pad = static_cast<int>(V_pad);
-    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
-    p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
-    p.group_m = llp::kGroupM;
-    p.bias = bias;
-    p.targets = reinterpret_cast<const long long*>(targets);
-    p.temperature = temperature;
-    p.ignore_index = ignore_index;
-    p.grad_logp = grad_logp;
-    p.lse = saved_lse;
-    p.dz = dz;
-    p.gb_part = want_gb ? reinterpret_cast<float*>(ws + L.gb_part) : nullptr;
-    p.err = dev->status_ptr;
-    const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
-    rec_mark(s, -1);
-    if (llp::launch_dlogits(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
-    rec_mark(s, kKDlogits);
-  }
-
-  // B2: grad_hidden = dz . W over fixed vocab segments
-  if (grad_hidden != nullptr) {
-    CUtensorMap tm_dz, tm_w_mn;
-    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
-    llp::GradGemmParams p;
-    p.rows = static_cast<int>(N);
-    p.D = static_cast<int>(D);
-    p.K = static_cast<int>(V);
-    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
-    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
-    p.nseg = static_cast<int>(cdiv(V, llp::kKSegment));
-    p.kseg_blocks = llp::kKSegment / llp::kTileK;
-    p.out = static_cast<__nv_bfloat16*>(grad_hidden);
-    p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
-    p.err = dev->status_ptr;
-    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
-    if (llp::launch_grad_hidden(tm_dz, tm_w_mn, p, units, dev->caps, s) != cudaSuccess)
+int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                            const float* bias, const int64_t* targets, const float* temperature, int64_t N,
+                            int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
+                            void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  int st = check_shapes(N, D, V);
+  if (st != LLP_OK) return st;
+  if (K < 0 || K > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (grad_bias != nullptr && bias == nullptr) return LLP_ERR_NULL_POINTER;
+  if ((grad_hidden && !aligned(grad_hidden, 16)) || (grad_weight && !aligned(grad_weight, 16)) ||
+      (grad_bias && !aligned(grad_bias, 4)))
+    return LLP_ERR_MISALIGNED;
+  if (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr) return LLP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInit* dev = nullptr;
+  if (N == 0 || K == 0) {  // nothing selected: every gradient is zero
+    if ((st = init_device(&dev)) != LLP_OK) return st;
+    if (grad_hidden && N > 0 && cudaMemsetAsync(grad_hidden, 0, static_cast<size_t>(N) * D * 2, s) != cudaSuccess)
       return LLP_ERR_CUDA;
-    rec_mark(s, kKGradHidden);
-    if (p.nseg > 1) {
-      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s) != cudaSuccess)
-        return LLP_ERR_CUDA;
-      rec_mark(s, kKSegSumHidden);
-    }
-  }
-
-  // B3: grad_weight = dz^T . h over fixed token segments
-  if (grad_weight != nullptr) {
-    CUtensorMap tm_dz_mn, tm_h_mn;
-    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
-    llp::GradGemmParams p;
-    p.rows = static_cast<int>(V);
-    p.D = static_cast<int>(D);
-    p.K = static_cast<int>(N);
-    p.num_m = static_cast<int>(cdiv(V, llp::kUnitM));
-    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
-    p.nseg = static_cast<int>(cdiv(N, llp::kKSegment));
-    p.kseg_blocks = llp::kKSegment / llp::kTileK;
-    p.out = static_cast<__nv_bfloat16*>(grad_weight);
-    p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
-    p.err = dev->status_ptr;
-    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
-    if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, p, units, dev->caps, s) != cudaSuccess)
+    if (grad_weight && cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * D * 2, s) != cudaSuccess)
       return LLP_ERR_CUDA;
-    rec_mark(s, kKGradWeight);
-    if (p.nseg > 1) {
-      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s) != cudaSuccess)
-        return LLP_ERR_CUDA;
-      rec_mark(s, kKSegSumWeight);
-    }
-  }
-
-  // B4: grad_bias
-  if (want_gb) {
-    const int nblocks = static_cast<int>(cdiv(N, llp::kUnitM) * (llp::kUnitM / 32));
-    if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
-                             s) != cudaSuccess)
+    if (grad_bias && cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(V) * 4, s) != cudaSuccess)
       return LLP_ERR_CUDA;
-    rec_mark(s, kKBiasSum);
+    return LLP_OK;
   }
+  if (indices == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(indices, 8)) return LLP_ERR_MISALIGNED;
+  st = check_inputs(hidden, weight, bias, targets, temperature, N, D, V);
+  if (st != LLP_OK) return st;
+  if (grad_logp == nullptr || saved_lse == nullptr || workspace == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(grad_logp, 4) || !aligned(saved_lse, 4) || !aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
+  const IdxLayout L = idx_layout(N, D, V, K, true, bias != nullptr);
+  if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  llp::RowSelection sel;
+  if (llp::build_row_selection(reinterpret_cast<const long long*>(indices), K, static_cast<int>(N), ws + L.sel, &sel,
+                               s) != cudaSuccess)
+    return LLP_ERR_CUDA;
+  auto* c_hidden = reinterpret_cast<__nv_bfloat16*>(ws + L.c_hidden);
+  auto* c_targets = reinterpret_cast<long long*>(ws + L.c_targets);
+  float* c_temp = temperature ? reinterpret_cast<float*>(ws + L.c_temp) : nullptr;
+  float* c_grad = reinterpret_cast<float*>(ws + L.c_a);
+  float* c_lse = reinterpret_cast<float*>(ws + L.c_b);
+  if (llp::gather_selected_rows(sel, static_cast<int>(D), static_cast<const __nv_bfloat16*>(hidden),
+                                reinterpret_cast<const long long*>(targets), temperature, grad_logp, saved_lse,
+                                ignore_index, c_hidden, c_targets, c_temp, c_grad, c_lse, s) != cudaSuccess)
+    return LLP_ERR_CUDA;
+  auto* c_gh = grad_hidden ? reinterpret_cast<__nv_bfloat16*>(ws + L.c_gh) : nullptr;
+  st = bwd_core(dev, c_grad, c_lse, c_hidden, weight, bias, reinterpret_cast<const int64_t*>(c_targets), c_temp,
+                L.Kc, D, V, ignore_index, c_gh, grad_weight, grad_bias, ws + L.inner, s);
+  if (st != LLP_OK) return st;
+  if (grad_hidden &&
+      llp::scatter_selected_grad_hidden(sel, static_cast<int>(N), static_cast<int>(D), c_gh,
+                                        static_cast<__nv_bfloat16*>(grad_hidden), s) != cudaSuccess)
+    return LLP_ERR_CUDA;
   return LLP_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Logits-input fused log-prob (include/fused_logp.h).
+// ----------------------------------------------------------------------------
+static int fused_check(const void* logits, int dtype, int64_t N, int64_t V, const int64_t* targets) {
+  if (dtype != FUSED_LOGP_DTYPE_BF16 && dtype != FUSED_LOGP_DTYPE_F32) return LLP_ERR_BAD_SHAPE;
+  if (N < 0 || V < 1 || N > kLim31 || V > kLim31 || !product_ok(N, V)) return LLP_ERR_BAD_SHAPE;
+  if (N * cdiv(V, llp::kLogitsSplit) > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (N == 0) return LLP_OK;
+  if (logits == nullptr || targets == nullptr) return LLP_ERR_NULL_POINTER;
+  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_BF16 ? 2 : 4;
+  if (!aligned(logits, es) || !aligned(targets, 8)) return LLP_ERR_MISALIGNED;
+  return LLP_OK;
+}
+
+static bool fused_vec_ok(const void* p, int dtype, int64_t V) {
+  const int64_t es = dtype == FUSED_LOGP_DTYPE_BF16 ? 2 : 4;
+  return aligned(p, 16) && ((V * es) % 16) == 0;
+}
+
+size_t fused_logp_workspace_bytes(int64_t N, int64_t V) {
+  if (N <= 0 || V < 1 || N > kLim31 || V > kLim31) return 0;
+  return static_cast<size_t>(2 * cdiv(V, llp::kLogitsSplit) * N) * sizeof(float);
+}
+
+int fused_logp_fwd(const void* logits, int dtype, int64_t N, int64_t V, const int64_t* targets,
+                   int64_t ignore_index, float* out_logp, float* out_row_max, float* out_log_sum, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  int st = fused_check(logits, dtype, N, V, targets);
+  if (st != LLP_OK) return st;
+  if (N == 0) return LLP_OK;
+  if (out_logp == nullptr || out_row_max == nullptr || out_log_sum == nullptr || workspace == nullptr)
+    return LLP_ERR_NULL_POINTER;
+  if (!aligned(out_logp, 4) || !aligned(out_row_max, 4) || !aligned(out_log_sum, 4) || !aligned(workspace, 16))
+    return LLP_ERR_MISALIGNED;
+  if (workspace_bytes < fused_logp_workspace_bytes(N, V)) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  const cudaError_t e = llp::launch_logits_fwd(
+      logits, dtype, static_cast<int>(N), static_cast<int>(V), reinterpret_cast<const long long*>(targets),
+      ignore_index, static_cast<float*>(workspace), out_logp, out_row_max, out_log_sum,
+      fused_vec_ok(logits, dtype, V), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LLP_OK : LLP_ERR_CUDA;
+}
+
+int fused_logp_bwd(const float* grad_logp, const float* row_max, const float* log_sum, const void* logits, int dtype,
+                   int64_t N, int64_t V, const int64_t* targets, int64_t ignore_index, void* grad_logits,
+                   void* stream) {
+  int st = fused_check(logits, dtype, N, V, targets);
+  if (st != LLP_OK) return st;
+  if (N == 0) return LLP_OK;
+  if (grad_logp == nullptr || row_max == nullptr || log_sum == nullptr || grad_logits == nullptr)
+    return LLP_ERR_NULL_POINTER;
+  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_BF16 ? 2 : 4;
+  if (!aligned(grad_logp, 4) || !aligned(row_max, 4) || !aligned(log_sum, 4) || !aligned(grad_logits, es))
+    return LLP_ERR_MISALIGNED;
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  const bool vec = fused_vec_ok(logits, dtype, V) && fused_vec_ok(grad_logits, dtype, V);
+  const cudaError_t e = llp::launch_logits_bwd(
+      logits, dtype, static_cast<int>(N), static_cast<int>(V), reinterpret_cast<const long long*>(targets),
+      ignore_index, grad_logp, row_max, log_sum, grad_logits, vec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LLP_OK : LLP_ERR_CUDA;
+}
+
+// One thread waits, with the production wait code, on a barrier that nothing
+// ever completes; the bounded wait must give up after limit_ns and record the
+// self-test code instead of hanging.
+static __global__ void wait_timeout_probe_kernel(unsigned int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  llp::mbar_init(&bar, 1);
+  abort_flag = 0;
+  llp::fence_mbarrier_init();
+  llp::mbar_wait(&bar, 0, &abort_flag, err, llp::kDevTimeoutSelfTest, limit_ns);
+}
+
+int linear_logp_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns < 1 || limit_ns > 1000000000ull) return LLP_ERR_BAD_SHAPE;
+  DeviceInit* dev = nullptr;
+  const int st = init_device(&dev);
+  if (st != LLP_OK) return st;
+  wait_timeout_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(dev->status_ptr, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? LLP_OK : LLP_ERR_CUDA;
 }
 
 int linear_logp_device_status(void* stream, unsigned int* device_code) {

@@ -63,7 +63,7 @@ struct DzCfg {
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
   static constexpr int STAGES = PAIR ? kPairStages : 4;
-  static constexpr int EXTRA_SMEM = 0;
+  static constexpr int EXTRA_SMEM = kEpiSmemBytes;
   static constexpr int UM = kUnitM;
   using Params = DzParams;
 
@@ -115,57 +115,59 @@ struct DzCfg {
   }
 
   static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int, int row, int lane,
-                                              uint32_t taddr, RowState& rs) {
+                                              uint32_t taddr, RowState& rs, EpiStore& es) {
     const int v0 = ui.n0;
     const bool full = (v0 + BN) <= p.V;
     const int blk = (ui.m0 + row) >> 5;  // 32-row block of this warp
+    const int row0 = ui.m0 + row - lane;  // first token row of this warp's slab
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float z[32];
-      tmem_load_32cols(taddr + c * 32, z);
-      const int vc = v0 + c * 32;
-      if (HAS_BIAS) {
-        if (full) {
-          const float4* b4 = reinterpret_cast<const float4*>(p.bias + vc);
+    for (int q = 0; q < BN / 64; ++q) {  // 64-column slabs of dz, one TMA store each
+      if (v0 + 64 * q >= p.V) break;     // warp-uniform
+      const uint32_t sbuf = epi_slab_begin(es);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 b = __ldg(b4 + q);
-            z[4 * q + 0] += b.x;
-            z[4 * q + 1] += b.y;
-            z[4 * q + 2] += b.z;
-            z[4 * q + 3] += b.w;
+      for (int h = 0; h < 2; ++h) {
+        const int vc = v0 + 64 * q + 32 * h;
+        float z[32];
+        tmem_load_32cols(taddr + 64 * q + 32 * h, z);
+        if (HAS_BIAS) {
+          if (full) {
+            const float4* b4 = reinterpret_cast<const float4*>(p.bias + vc);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float4 b = __ldg(b4 + k);
+              z[4 * k + 0] += b.x;
+              z[4 * k + 1] += b.y;
+              z[4 * k + 2] += b.z;
+              z[4 * k + 3] += b.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] += (vc + i < p.V) ? __ldg(p.bias + vc + i) : 0.f;
           }
-        } else {
+        }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] += (vc + i < p.V) ? __ldg(p.bias + vc + i) : 0.f;
+        for (int i = 0; i < 32; ++i) {
+          const float zz = z[i] * rs.inv_tau;
+          const float pr = exp2f((zz - rs.lse) * kLog2eB);
+          const float oh = (vc + i == rs.t) ? 1.f : 0.f;
+          float d = rs.gs * (oh - pr);
+          if (!rs.valid || (!full && vc + i >= p.V)) d = 0.f;
+          z[i] = d;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          epi_slab_put(sbuf, lane, 4 * h + k, pack_bf16x2(z[8 * k + 0], z[8 * k + 1]),
+                       pack_bf16x2(z[8 * k + 2], z[8 * k + 3]), pack_bf16x2(z[8 * k + 4], z[8 * k + 5]),
+                       pack_bf16x2(z[8 * k + 6], z[8 * k + 7]));
+        if (HAS_BIAS && p.gb_part != nullptr) {  // warp-uniform
+          const float colsum = warp_column_sums(z, lane);
+          const int v = vc + lane;
+          if (v < p.V) p.gb_part[static_cast<size_t>(blk) * p.V + v] = colsum;
         }
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float zz = z[i] * rs.inv_tau;
-        const float pr = exp2f((zz - rs.lse) * kLog2eB);
-        const float oh = (vc + i == rs.t) ? 1.f : 0.f;
-        float d = rs.gs * (oh - pr);
-        if (!rs.valid || (!full && vc + i >= p.V)) d = 0.f;
-        z[i] = d;
-      }
-      if (rs.n < p.N && vc < p.V_pad) {
-        uint4* dst = reinterpret_cast<uint4*>(p.dz + static_cast<size_t>(rs.n) * p.V_pad + vc);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16x2(z[8 * q + 0], z[8 * q + 1]);
-          w.y = pack_bf16x2(z[8 * q + 2], z[8 * q + 3]);
-          w.z = pack_bf16x2(z[8 * q + 4], z[8 * q + 5]);
-          w.w = pack_bf16x2(z[8 * q + 6], z[8 * q + 7]);
-          dst[q] = w;
-        }
-      }
-      if (HAS_BIAS && p.gb_part != nullptr) {  // warp-uniform
-        const float colsum = warp_column_sums(z, lane);
-        const int v = vc + lane;
-        if (v < p.V) p.gb_part[static_cast<size_t>(blk) * p.V + v] = colsum;
-      }
+      // rows >= N and columns >= V are clipped by the store's tensor map; a slab
+      // that starts past the last row is not stored at all (warp-uniform)
+      if (row0 < p.N) epi_slab_store_2d(es, sbuf, v0 + 64 * q, row0);
     }
   }
 
@@ -182,7 +184,7 @@ struct GradCfg {
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
   static constexpr int STAGES = PAIR ? kPairStages : 4;
-  static constexpr int EXTRA_SMEM = 0;
+  static constexpr int EXTRA_SMEM = kEpiSmemBytes;
   static constexpr int UM = kUnitM;
   using Params = GradGemmParams;
 
@@ -217,36 +219,45 @@ struct GradCfg {
     rs.r = ui.m0 + row;
   }
 
-  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int u, int, int, int,
-                                              uint32_t taddr, RowState& rs) {
+  // Output through 32-row slabs and TMA stores: bf16 [rows][D] with one
+  // segment, else the fp32 partial of this segment in [nseg][rows][D] (a 3-D
+  // tensor map, so rows past `rows` are clipped inside the segment).
+  static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int u, int, int row, int lane,
+                                              uint32_t taddr, RowState&, EpiStore& es) {
     const int seg = u / (p.num_m * p.num_d);
+    const int row0 = ui.m0 + row - lane;
+    if (row0 >= p.rows) return;  // this warp's rows are all past the end (warp-uniform)
+    if (p.nseg == 1) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int d0 = ui.n0 + c * 32;
-      if (d0 >= p.D) break;  // warp-uniform
-      float a[32];
-      tmem_load_32cols(taddr + c * 32, a);
-      if (rs.r >= p.rows) continue;
-      if (p.nseg == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(rs.r) * p.D + d0);
+      for (int q = 0; q < BN / 64; ++q) {
+        const int d0 = ui.n0 + 64 * q;
+        if (d0 >= p.D) break;  // warp-uniform
+        const uint32_t sbuf = epi_slab_begin(es);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (d0 + 8 * q < p.D) {
-            uint4 w;
-            w.x = pack_bf16x2(a[8 * q + 0], a[8 * q + 1]);
-            w.y = pack_bf16x2(a[8 * q + 2], a[8 * q + 3]);
-            w.z = pack_bf16x2(a[8 * q + 4], a[8 * q + 5]);
-            w.w = pack_bf16x2(a[8 * q + 6], a[8 * q + 7]);
-            dst[q] = w;
-          }
-        }
-      } else {
-        float4* dst =
-            reinterpret_cast<float4*>(p.part + (static_cast<size_t>(seg) * p.rows + rs.r) * p.D + d0);
+        for (int h = 0; h < 2; ++h) {
+          float a[32];
+          tmem_load_32cols(taddr + 64 * q + 32 * h, a);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (d0 + 4 * q < p.D) dst[q] = make_float4(a[4 * q + 0], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+          for (int k = 0; k < 4; ++k)
+            epi_slab_put(sbuf, lane, 4 * h + k, pack_bf16x2(a[8 * k + 0], a[8 * k + 1]),
+                         pack_bf16x2(a[8 * k + 2], a[8 * k + 3]), pack_bf16x2(a[8 * k + 4], a[8 * k + 5]),
+                         pack_bf16x2(a[8 * k + 6], a[8 * k + 7]));
         }
+        epi_slab_store_2d(es, sbuf, d0, row0);
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int d0 = ui.n0 + 32 * c;
+        if (d0 >= p.D) break;  // warp-uniform
+        const uint32_t sbuf = epi_slab_begin(es);
+        float a[32];
+        tmem_load_32cols(taddr + 32 * c, a);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          epi_slab_put(sbuf, lane, k, __float_as_uint(a[4 * k + 0]), __float_as_uint(a[4 * k + 1]),
+                       __float_as_uint(a[4 * k + 2]), __float_as_uint(a[4 * k + 3]));
+        epi_slab_store_3d(es, sbuf, d0, row0, seg);
       }
     }
   }
@@ -285,10 +296,10 @@ __global__ void __launch_bounds__(256) bias_sum_kernel(const float* __restrict__
 }
 
 template <class Cfg>
-static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p,
-                                long long units, int groups, cudaStream_t s) {
+static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                                const typename Cfg::Params& p, long long units, int groups, cudaStream_t s) {
   const long long g = units < groups ? units : groups;
-  return launch_gemm<Cfg>(a, b, p, static_cast<int>(g) * Plan<Cfg>::NCTA, s);
+  return launch_gemm<Cfg>(a, b, c, p, static_cast<int>(g) * Plan<Cfg>::NCTA, s);
 }
 
 cudaError_t bwd_setup(LaunchCaps* caps) {
@@ -299,20 +310,20 @@ cudaError_t bwd_setup(LaunchCaps* caps) {
   return setup_gemm<GradCfg<true, true>>(&caps->gw_groups);
 }
 
-cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, long long units,
-                           const LaunchCaps& caps, cudaStream_t s) {
-  return p.bias ? launch_units<DzCfg<true>>(tm_h, tm_w, p, units, caps.dz_groups[1], s)
-                : launch_units<DzCfg<false>>(tm_h, tm_w, p, units, caps.dz_groups[0], s);
+cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_dz_out,
+                           const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s) {
+  return p.bias ? launch_units<DzCfg<true>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_groups[1], s)
+                : launch_units<DzCfg<false>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_groups[0], s);
 }
 
-cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const GradGemmParams& p,
-                               long long units, const LaunchCaps& caps, cudaStream_t s) {
-  return launch_units<GradCfg<false, true>>(tm_dz, tm_w_mn, p, units, caps.gh_groups, s);
+cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const CUtensorMap& tm_out,
+                               const GradGemmParams& p, long long units, const LaunchCaps& caps, cudaStream_t s) {
+  return launch_units<GradCfg<false, true>>(tm_dz, tm_w_mn, tm_out, p, units, caps.gh_groups, s);
 }
 
-cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const GradGemmParams& p,
-                               long long units, const LaunchCaps& caps, cudaStream_t s) {
-  return launch_units<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, p, units, caps.gw_groups, s);
+cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const CUtensorMap& tm_out,
+                               const GradGemmParams& p, long long units, const LaunchCaps& caps, cudaStream_t s) {
+  return launch_units<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, tm_out, p, units, caps.gw_groups, s);
 }
 
 cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s) {

@@ -87,7 +87,7 @@ struct FwdCfg {
   }
 
   static __device__ __forceinline__ void tile(const Params& p, const UnitInfo& ui, int, int j, int, int,
-                                              uint32_t taddr, RowState& rs) {
+                                              uint32_t taddr, RowState& rs, EpiStore&) {
     const int v0 = ui.n0 + j * BN;
     const bool full = (v0 + BN) <= p.V;
     const int tl = rs.tloc - j * BN;
@@ -182,7 +182,7 @@ template <class Cfg>
 static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p,
                                 long long units, int groups, cudaStream_t s) {
   const long long g = units < groups ? units : groups;
-  return launch_gemm<Cfg>(a, b, p, static_cast<int>(g) * Plan<Cfg>::NCTA, s);
+  return launch_gemm<Cfg>(a, b, a, p, static_cast<int>(g) * Plan<Cfg>::NCTA, s);  // no tensor stores
 }
 
 cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,

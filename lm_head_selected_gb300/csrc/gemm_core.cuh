@@ -87,6 +87,57 @@ struct SharedState {
 };
 
 // ----------------------------------------------------------------------------
+// Epilogue output path: each epilogue warp stages 32-row x 128-byte slabs of
+// its accumulator rows in shared memory (two 4 KB buffers, 128-byte swizzled
+// exactly as the store's tensor map expects: 16-byte chunk c of row r sits at
+// chunk c ^ (r % 8)) and writes them with TMA tensor stores, so global writes
+// leave the SM as whole lines instead of 32 scattered 16-byte pieces.
+// ----------------------------------------------------------------------------
+constexpr int kEpiStageBytes = 4096;
+constexpr int kEpiSmemBytes = 4 * 2 * kEpiStageBytes;  // 4 epilogue warps x 2 buffers
+
+struct EpiStore {
+  const CUtensorMap* map;
+  uint32_t buf0;  // this warp's first staging buffer (shared address, 1024-aligned)
+  uint32_t next;  // buffer the next slab goes to
+  int lane;
+};
+
+// Returns the staging buffer for the next slab once its previous store has read it.
+__device__ __forceinline__ uint32_t epi_slab_begin(EpiStore& es) {
+  if (es.lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  return es.buf0 + es.next * kEpiStageBytes;
+}
+
+// This lane's 16-byte chunk c (0..7) of its slab row.
+__device__ __forceinline__ void epi_slab_put(uint32_t buf, int lane, int c, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  const uint32_t addr = buf + lane * 128 + ((static_cast<uint32_t>(c) ^ (lane & 7)) << 4);
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ void epi_slab_store_2d(EpiStore& es, uint32_t buf, int x, int y) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (es.lane == 0) {
+    tma_store_2d(es.map, buf, x, y);
+    bulk_commit_group();
+  }
+  es.next ^= 1u;
+}
+
+__device__ __forceinline__ void epi_slab_store_3d(EpiStore& es, uint32_t buf, int x, int y, int z) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (es.lane == 0) {
+    tma_store_3d(es.map, buf, x, y, z);
+    bulk_commit_group();
+  }
+  es.next ^= 1u;
+}
+
+// ----------------------------------------------------------------------------
 // Producer: one lane of warp 0 in every CTA.
 // ----------------------------------------------------------------------------
 template <class Cfg>
@@ -216,25 +267,35 @@ __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cf
 // Epilogue: warps 2..5 of every CTA.
 // ----------------------------------------------------------------------------
 template <class Cfg>
-__device__ __forceinline__ void run_epilogue(const SharedState& st, const typename Cfg::Params& p) {
+__device__ __forceinline__ void run_epilogue(const SharedState& st, const CUtensorMap* tmC,
+                                             const typename Cfg::Params& p) {
   using P = Plan<Cfg>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = warp & 3;                                          // TMEM lane group of this warp
   const int row = static_cast<int>(st.rank) * BM + g * 32 + lane;  // accumulator row within the unit
+  EpiStore es;
+  es.map = tmC;
+  es.buf0 = smem_u32(st.extra) + static_cast<uint32_t>(g) * 2u * kEpiStageBytes;
+  es.next = 0;
+  es.lane = lane;
   uint32_t acc_i = 0;
+  bool ok = true;
   const int num_units = Cfg::num_units(p);
-  for (int u = st.unit_first; u < num_units; u += st.unit_stride) {
+  for (int u = st.unit_first; ok && u < num_units; u += st.unit_stride) {
     const UnitInfo ui = Cfg::unit(p, u);
     typename Cfg::RowState rs;
     Cfg::unit_begin(p, ui, u, row, rs);
     for (int j = 0; j < ui.ntiles; ++j, ++acc_i) {
       const uint32_t buf = acc_i & 1u;
       const uint32_t acc_phase = (acc_i >> 1) & 1u;
-      if (!mbar_wait(&st.tmem_full[buf], acc_phase, st.abort, st.err, kDevTimeoutTmemFull)) return;
+      if (!mbar_wait(&st.tmem_full[buf], acc_phase, st.abort, st.err, kDevTimeoutTmemFull)) {
+        ok = false;
+        break;
+      }
       tc_fence_after_sync();
       const uint32_t taddr = st.tmem_base + (static_cast<uint32_t>(g * 32) << 16) + buf * Cfg::BN;
-      Cfg::tile(p, ui, u, j, row, lane, taddr, rs);
+      Cfg::tile(p, ui, u, j, row, lane, taddr, rs, es);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -244,14 +305,17 @@ __device__ __forceinline__ void run_epilogue(const SharedState& st, const typena
           mbar_arrive(&st.tmem_empty[buf]);
       }
     }
-    Cfg::unit_end(p, ui, u, row, rs);
+    if (ok) Cfg::unit_end(p, ui, u, row, rs);
   }
+  // every tensor store of this warp must be complete before the CTA exits
+  if (lane == 0) bulk_wait_group_all();
+  __syncwarp();
 }
 
 template <class Cfg>
 __global__ void __launch_bounds__(kNumThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const typename Cfg::Params p) {
+                   const __grid_constant__ CUtensorMap tmC, const typename Cfg::Params p) {
   using P = Plan<Cfg>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -290,6 +354,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (Cfg::EXTRA_SMEM > 0) tma_prefetch_desc(&tmC);
   }
   __syncwarp();  // the .aligned barriers and tcgen05 allocation below need converged warps
   if (warp == 1) {
@@ -325,7 +390,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (!mbar_wait_drain(st.drain, 0, 100000000ull)) atomicCAS(st.err, 0u, kDevTimeoutDrain);
     }
   } else {
-    run_epilogue<Cfg>(st, p);
+    run_epilogue<Cfg>(st, &tmC, p);
   }
 
   tc_fence_before_sync();
@@ -347,8 +412,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
 // Launch helper: pair configurations run as 2-CTA clusters.
 template <class Cfg>
-inline cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const typename Cfg::Params& p, int grid,
-                               cudaStream_t s) {
+inline cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                               const typename Cfg::Params& p, int grid, cudaStream_t s) {
   using P = Plan<Cfg>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -362,7 +427,7 @@ inline cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Cfg>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Cfg>, a, b, c, p);
 }
 
 // One-time set-up per kernel: shared-memory opt-in and the number of clusters

@@ -84,12 +84,51 @@ cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s);
 
 cudaError_t bwd_setup(LaunchCaps* caps);
-cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DzParams& p, long long units,
-                           const LaunchCaps& caps, cudaStream_t s);
-cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const GradGemmParams& p,
-                               long long units, const LaunchCaps& caps, cudaStream_t s);
-cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const GradGemmParams& p,
-                               long long units, const LaunchCaps& caps, cudaStream_t s);
+// The third tensor map is the output the epilogue stores through: dz (bf16,
+// box 64 x 32), or the gradient (bf16, box 64 x 32) / its fp32 segment
+// partials ([nseg][rows][D], box 32 x 32 x 1).
+cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_dz_out,
+                           const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s);
+cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const CUtensorMap& tm_out,
+                               const GradGemmParams& p, long long units, const LaunchCaps& caps, cudaStream_t s);
+cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const CUtensorMap& tm_out,
+                               const GradGemmParams& p, long long units, const LaunchCaps& caps, cudaStream_t s);
+// Logits-input fused log-prob (logits.cu).  dtype: kDtypeBF16 or kDtypeF32.
+// `part` holds 2 * ceil(V / kLogitsSplit) * N floats.  `vec` = rows are 16-byte
+// aligned (base and row pitch), so 16-byte loads and stores may be used.
+constexpr int kDtypeBF16 = 0;
+constexpr int kDtypeF32 = 1;
+constexpr int kLogitsSplit = 16384;  // vocab elements per CTA (fixed: depends on nothing)
+cudaError_t launch_logits_fwd(const void* z, int dtype, int N, int V, const long long* targets,
+                              long long ignore_index, float* part, float* logp, float* row_max, float* log_sum,
+                              bool vec, cudaStream_t s);
+cudaError_t launch_logits_bwd(const void* z, int dtype, int N, int V, const long long* targets,
+                              long long ignore_index, const float* grad_logp, const float* row_max,
+                              const float* log_sum, void* grad, bool vec, cudaStream_t s);
+
+// Row selection for the indexed variants (indexed.cu): the index list becomes a
+// byte mask over N rows and the selected rows, in ascending order, padded with
+// -1 up to K = min(#indices, N) slots.  `total` (device) = number of rows selected.
+struct RowSelection {
+  unsigned char* mask;  // [N]
+  int* rows;            // [K]
+  int* slot_of;         // [N], valid where mask != 0
+  int* total;           // device scalar
+  int K;
+};
+size_t select_workspace_bytes(long long N, long long K);
+cudaError_t build_row_selection(const long long* idx, long long K, int N, void* ws, RowSelection* sel,
+                                cudaStream_t s);
+cudaError_t gather_selected_rows(const RowSelection& sel, int D, const __nv_bfloat16* hidden,
+                                 const long long* targets, const float* temperature, const float* grad_logp,
+                                 const float* lse, long long ignore_index, __nv_bfloat16* c_hidden,
+                                 long long* c_targets, float* c_temperature, float* c_grad, float* c_lse,
+                                 cudaStream_t s);
+cudaError_t scatter_selected_outputs(const RowSelection& sel, const float* c_logp, const float* c_lse, float* logp,
+                                     float* lse, cudaStream_t s);
+cudaError_t scatter_selected_grad_hidden(const RowSelection& sel, int N, int D, const __nv_bfloat16* c_gh,
+                                         __nv_bfloat16* gh, cudaStream_t s);
+
 cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s);
 cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s);
 

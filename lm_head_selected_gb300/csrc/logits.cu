@@ -1,0 +1,293 @@
+// Logits-input fused log-probability ("Fused LogP": the logits [N, V] are
+// already materialised; "add backward support for fused logp CUDA kernels",
+// Summary and Implementation details).
+//
+//   forward   per (row, 16384-wide vocab split) CTA: stream the split once with
+//             16-byte loads, keep a per-thread (max, sum of exp) pair, merge the
+//             pairs in a fixed tree order -> partial (m_s, s_s);
+//             then per row: merge the splits in ascending order, read z[t] once,
+//             row_max = M, log_sum = log S, logp = (z[t] - M) - log S.
+//   backward  per (row, split) CTA: grad[v] = g * (onehot(t)[v] - exp((z[v] -
+//             row_max) - log_sum)) written in the logits' dtype, zero rows for
+//             invalid targets; no probability tensor is formed.
+//
+// Both are bound by HBM bandwidth (every logit read once; the backward also
+// writes every gradient once).  The split width and the reduction trees depend
+// on V only, so a row's results are the same for every N and every run.
+#include <cuda_bf16.h>
+
+#include "llp_internal.h"
+
+namespace llp {
+
+namespace {
+
+constexpr int kLThreads = 256;
+constexpr float kLog2eL = 1.4426950408889634f;
+
+__device__ __forceinline__ bool tgt_ok(long long t, int V, long long ignore_index) {
+  return t != ignore_index && t >= 0 && t < static_cast<long long>(V);
+}
+
+// 16-byte vector of logits converted to fp32.
+template <int DT>
+struct Vec;
+template <>
+struct Vec<kDtypeBF16> {
+  static constexpr int W = 8;
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ void load(const T* p, float (&v)[W]) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  static __device__ __forceinline__ float load1(const T* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ void store(T* p, const float (&v)[W]) {
+    uint4 r;
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]),
+                   c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
+    r.x = *reinterpret_cast<uint32_t*>(&a);
+    r.y = *reinterpret_cast<uint32_t*>(&b);
+    r.z = *reinterpret_cast<uint32_t*>(&c);
+    r.w = *reinterpret_cast<uint32_t*>(&d);
+    *reinterpret_cast<uint4*>(p) = r;
+  }
+  static __device__ __forceinline__ void store1(T* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+template <>
+struct Vec<kDtypeF32> {
+  static constexpr int W = 4;
+  using T = float;
+  static __device__ __forceinline__ void load(const T* p, float (&v)[W]) {
+    const float4 r = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = r.x;
+    v[1] = r.y;
+    v[2] = r.z;
+    v[3] = r.w;
+  }
+  static __device__ __forceinline__ float load1(const T* p) { return __ldg(p); }
+  static __device__ __forceinline__ void store(T* p, const float (&v)[W]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  static __device__ __forceinline__ void store1(T* p, float v) { *p = v; }
+};
+
+// Merge (m, s) pairs: s is a sum of exp(x - m).
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;  // both empty
+  s = s * exp2f((m - mn) * kLog2eL) + s2 * exp2f((m2 - mn) * kLog2eL);
+  m = mn;
+}
+
+// Fixed-order block reduction of the per-thread pairs (butterfly within warps,
+// then warp 0 over the warps in ascending order).
+__device__ __forceinline__ void block_merge(float& m, float& s, float* sm_m, float* sm_s) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge_ms(m, s, m2, s2);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_s[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = sm_m[0], S = sm_s[0];
+    for (int w = 1; w < kLThreads / 32; ++w) merge_ms(M, S, sm_m[w], sm_s[w]);
+    sm_m[0] = M;
+    sm_s[0] = S;
+  }
+  __syncthreads();
+  m = sm_m[0];
+  s = sm_s[0];
+}
+
+// Each thread owns elements [split0 + (it * kLThreads + tid) * W, + W) for it = 0..ITERS-1.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kLThreads) logits_split_kernel(const typename Vec<DT>::T* __restrict__ z, int N,
+                                                                 int V, int S, float* __restrict__ part_m,
+                                                                 float* __restrict__ part_s) {
+  using VV = Vec<DT>;
+  constexpr int W = VV::W;
+  constexpr int ITERS = kLogitsSplit / (kLThreads * W);
+  __shared__ float sm_m[kLThreads / 32], sm_s[kLThreads / 32];
+  const long long cta = blockIdx.x;
+  const int row = static_cast<int>(cta / S);
+  const int split = static_cast<int>(cta - static_cast<long long>(row) * S);
+  const int v0 = split * kLogitsSplit;
+  const typename VV::T* zr = z + static_cast<size_t>(row) * V;
+  float vals[ITERS][W];
+#pragma unroll
+  for (int it = 0; it < ITERS; ++it) {
+    const int v = v0 + (it * kLThreads + threadIdx.x) * W;
+    if (VEC && v + W <= V) {
+      VV::load(zr + v, vals[it]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; ++k) vals[it][k] = (v + k < V) ? VV::load1(zr + v + k) : -INFINITY;
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int it = 0; it < ITERS; ++it)
+#pragma unroll
+    for (int k = 0; k < W; ++k) m = fmaxf(m, vals[it][k]);
+  float s = 0.f;
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it)
+#pragma unroll
+      for (int k = 0; k < W; ++k) s += exp2f((vals[it][k] - m) * kLog2eL);
+  }
+  block_merge(m, s, sm_m, sm_s);
+  if (threadIdx.x == 0) {
+    part_m[static_cast<size_t>(split) * N + row] = m;
+    part_s[static_cast<size_t>(split) * N + row] = s;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) logits_merge_kernel(const typename Vec<DT>::T* __restrict__ z, int N, int V,
+                                                           int S, const long long* __restrict__ targets,
+                                                           long long ignore_index, const float* __restrict__ part_m,
+                                                           const float* __restrict__ part_s, float* __restrict__ logp,
+                                                           float* __restrict__ row_max, float* __restrict__ log_sum) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const long long t = targets[n];
+  if (!tgt_ok(t, V, ignore_index)) {
+    logp[n] = 0.f;
+    row_max[n] = -INFINITY;
+    log_sum[n] = 0.f;
+    return;
+  }
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[static_cast<size_t>(s) * N + n]);
+  float Ssum = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const size_t i = static_cast<size_t>(s) * N + n;
+    Ssum += part_s[i] * exp2f((part_m[i] - M) * kLog2eL);
+  }
+  const float ls = logf(Ssum);
+  const float zt = Vec<DT>::load1(z + static_cast<size_t>(n) * V + t);
+  row_max[n] = M;
+  log_sum[n] = ls;
+  logp[n] = (zt - M) - ls;
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kLThreads) logits_grad_kernel(const typename Vec<DT>::T* __restrict__ z, int N,
+                                                                int V, int S, const long long* __restrict__ targets,
+                                                                long long ignore_index,
+                                                                const float* __restrict__ grad_logp,
+                                                                const float* __restrict__ row_max,
+                                                                const float* __restrict__ log_sum,
+                                                                typename Vec<DT>::T* __restrict__ grad) {
+  using VV = Vec<DT>;
+  constexpr int W = VV::W;
+  constexpr int ITERS = kLogitsSplit / (kLThreads * W);
+  const long long cta = blockIdx.x;
+  const int row = static_cast<int>(cta / S);
+  const int split = static_cast<int>(cta - static_cast<long long>(row) * S);
+  const int v0 = split * kLogitsSplit;
+  const typename VV::T* zr = z + static_cast<size_t>(row) * V;
+  typename VV::T* gr = grad + static_cast<size_t>(row) * V;
+  const long long t = targets[row];
+  const bool ok = tgt_ok(t, V, ignore_index);
+  const float g = ok ? grad_logp[row] : 0.f;
+  const float m = ok ? row_max[row] : 0.f;
+  const float ls = ok ? log_sum[row] : 0.f;
+#pragma unroll 2
+  for (int it = 0; it < ITERS; ++it) {
+    const int v = v0 + (it * kLThreads + threadIdx.x) * W;
+    if (v >= V) break;
+    float x[W];
+    const bool vec = VEC && v + W <= V;
+    if (vec) {
+      VV::load(zr + v, x);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; ++k) x[k] = (v + k < V) ? VV::load1(zr + v + k) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const float p = exp2f(((x[k] - m) - ls) * kLog2eL);
+      const float oh = (static_cast<long long>(v + k) == t) ? 1.f : 0.f;
+      x[k] = ok ? g * (oh - p) : 0.f;
+    }
+    if (vec) {
+      VV::store(gr + v, x);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+        if (v + k < V) VV::store1(gr + v + k, x[k]);
+    }
+  }
+}
+
+template <int DT>
+cudaError_t launch_fwd_dt(const void* z, int N, int V, const long long* targets, long long ignore_index, float* part,
+                          float* logp, float* row_max, float* log_sum, bool vec, cudaStream_t s) {
+  using T = typename Vec<DT>::T;
+  const int S = (V + kLogitsSplit - 1) / kLogitsSplit;
+  float* pm = part;
+  float* ps = part + static_cast<size_t>(S) * N;
+  const long long ctas = static_cast<long long>(N) * S;
+  if (vec)
+    logits_split_kernel<DT, true><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(static_cast<const T*>(z), N, V, S,
+                                                                                    pm, ps);
+  else
+    logits_split_kernel<DT, false><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(static_cast<const T*>(z), N, V,
+                                                                                     S, pm, ps);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  logits_merge_kernel<DT><<<(N + 255) / 256, 256, 0, s>>>(static_cast<const T*>(z), N, V, S, targets, ignore_index, pm,
+                                                          ps, logp, row_max, log_sum);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_bwd_dt(const void* z, int N, int V, const long long* targets, long long ignore_index,
+                          const float* grad_logp, const float* row_max, const float* log_sum, void* grad, bool vec,
+                          cudaStream_t s) {
+  using T = typename Vec<DT>::T;
+  const int S = (V + kLogitsSplit - 1) / kLogitsSplit;
+  const long long ctas = static_cast<long long>(N) * S;
+  if (vec)
+    logits_grad_kernel<DT, true><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(
+        static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, static_cast<T*>(grad));
+  else
+    logits_grad_kernel<DT, false><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(
+        static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, static_cast<T*>(grad));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_logits_fwd(const void* z, int dtype, int N, int V, const long long* targets,
+                              long long ignore_index, float* part, float* logp, float* row_max, float* log_sum,
+                              bool vec, cudaStream_t s) {
+  return dtype == kDtypeBF16 ? launch_fwd_dt<kDtypeBF16>(z, N, V, targets, ignore_index, part, logp, row_max,
+                                                         log_sum, vec, s)
+                             : launch_fwd_dt<kDtypeF32>(z, N, V, targets, ignore_index, part, logp, row_max, log_sum,
+                                                        vec, s);
+}
+
+cudaError_t launch_logits_bwd(const void* z, int dtype, int N, int V, const long long* targets,
+                              long long ignore_index, const float* grad_logp, const float* row_max,
+                              const float* log_sum, void* grad, bool vec, cudaStream_t s) {
+  return dtype == kDtypeBF16 ? launch_bwd_dt<kDtypeBF16>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum,
+                                                         grad, vec, s)
+                             : launch_bwd_dt<kDtypeF32>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum,
+                                                        grad, vec, s);
+}
+
+}  // namespace llp

@@ -151,6 +151,60 @@ def linear_logp_bwd(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hidden: to
     return gh, gw, gb
 
 
+def _check_indices(indices: torch.Tensor, device) -> torch.Tensor:
+    if not isinstance(indices, torch.Tensor) or indices.dtype != torch.int64 or indices.device != device:
+        raise TypeError("indices must be an int64 tensor on the inputs' device")
+    return indices.reshape(-1).contiguous()
+
+
+def linear_logp_fwd_indexed(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                            indices: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                            temperature: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,
+                            out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """Forward on the rows named by ``indices`` only (duplicates count once, out of
+    range ignored).  Selected rows of ``out`` get the plain forward's values; the
+    others keep their contents (new buffers start as logp 0 / lse -inf)."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    idx = _check_indices(indices, dev)
+    lib = _lib.load()
+    if out is None:
+        logp = torch.zeros(N, dtype=torch.float32, device=dev)
+        lse = torch.full((N,), float("-inf"), dtype=torch.float32, device=dev)
+    else:
+        logp, lse = out
+    K = idx.numel()
+    ws = _workspace(int(lib.linear_logp_fwd_indexed_workspace_bytes(N, D, V, K)), dev, None)
+    st = lib.linear_logp_fwd_indexed(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), _ptr(temperature),
+                                     N, D, V, int(ignore_index), _ptr(idx), K, _ptr(logp), _ptr(lse), _ptr(ws),
+                                     ws.numel(), _stream(dev))
+    _lib.check("linear_logp_fwd_indexed", st)
+    return logp, lse
+
+
+def linear_logp_bwd_indexed(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hidden: torch.Tensor,
+                            weight: torch.Tensor, targets: torch.Tensor, indices: torch.Tensor,
+                            bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
+                            ignore_index: int = IGNORE_INDEX, need_hidden: bool = True, need_weight: bool = True,
+                            need_bias: bool = True):
+    """Gradients of the sum over the selected rows of grad_logp * logp; grad_hidden
+    rows that are not selected are zero."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    idx = _check_indices(indices, dev)
+    _need(grad_logp, "grad_logp", torch.float32, dev, 1)
+    _need(saved_lse, "saved_lse", torch.float32, dev, 1)
+    lib = _lib.load()
+    gh = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if need_hidden else None
+    gw = torch.empty((V, D), dtype=torch.bfloat16, device=dev) if need_weight else None
+    gb = torch.empty(V, dtype=torch.float32, device=dev) if (need_bias and bias is not None) else None
+    K = idx.numel()
+    ws = _workspace(int(lib.linear_logp_bwd_indexed_workspace_bytes(N, D, V, K, int(bias is not None))), dev, None)
+    st = lib.linear_logp_bwd_indexed(_ptr(grad_logp), _ptr(saved_lse), _ptr(hidden), _ptr(weight), _ptr(bias),
+                                     _ptr(targets), _ptr(temperature), N, D, V, int(ignore_index), _ptr(idx), K,
+                                     _ptr(gh), _ptr(gw), _ptr(gb), _ptr(ws), ws.numel(), _stream(dev))
+    _lib.check("linear_logp_bwd_indexed", st)
+    return gh, gw, gb
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the kernel status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

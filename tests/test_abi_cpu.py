@@ -122,6 +122,54 @@ def test_bwd_rejects_bad_arguments_on_host(lib):
     assert _bwd(lib, gh=0, gw=0, gb=0) == _lib.LLP_OK
 
 
+def test_fused_header_and_exports(lib):
+    with open(os.path.join(ROOT, "include", "fused_logp.h")) as f:
+        text = f.read()
+    names = set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\**\s+\**(fused_logp_[a-z_0-9]+)\s*\(", text, re.M))
+    assert names == set(_lib.EXPORTED_FUSED)
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_fused_rejects_bad_arguments_on_host(lib):
+    f = lambda x: P(x) if x else None  # noqa: E731
+    fwd = lambda **k: lib.fused_logp_fwd(  # noqa: E731
+        f(k.get("z", 0x1000)), k.get("dt", 0), k.get("N", 4), k.get("V", 100), f(k.get("t", 0x2000)), -100,
+        f(k.get("lp", 0x3000)), f(k.get("m", 0x4000)), f(k.get("ls", 0x5000)), f(k.get("ws", 0x6000)),
+        k.get("wsb", 1 << 20), None)
+    assert fwd(dt=2) == _lib.LLP_ERR_BAD_SHAPE
+    assert fwd(V=0) == _lib.LLP_ERR_BAD_SHAPE
+    assert fwd(z=0) == _lib.LLP_ERR_NULL_POINTER
+    assert fwd(t=0) == _lib.LLP_ERR_NULL_POINTER
+    assert fwd(lp=0) == _lib.LLP_ERR_NULL_POINTER
+    assert fwd(z=0x1001) == _lib.LLP_ERR_MISALIGNED
+    assert fwd(dt=1, z=0x1002) == _lib.LLP_ERR_MISALIGNED
+    assert fwd(wsb=lib.fused_logp_workspace_bytes(4, 100) - 1) == _lib.LLP_ERR_WORKSPACE_TOO_SMALL
+    assert fwd(N=0, z=0, t=0, lp=0, m=0, ls=0, ws=0) == _lib.LLP_OK
+    assert lib.fused_logp_workspace_bytes(16384, 131072) == 2 * 8 * 16384 * 4
+    assert lib.fused_logp_bwd(None, f(0x10), f(0x20), f(0x1000), 0, 4, 100, f(0x2000), -100, f(0x3000),
+                              None) == _lib.LLP_ERR_NULL_POINTER
+    assert lib.fused_logp_bwd(f(0x10), f(0x20), f(0x30), f(0x1000), 0, 4, 100, f(0x2000), -100, f(0x3001),
+                              None) == _lib.LLP_ERR_MISALIGNED
+
+
+def test_selftest_limit_is_checked_on_host(lib):
+    assert lib.linear_logp_selftest_wait_timeout(0, None) == _lib.LLP_ERR_BAD_SHAPE
+    assert lib.linear_logp_selftest_wait_timeout(2_000_000_000, None) == _lib.LLP_ERR_BAD_SHAPE
+
+
+def test_noalloc_limits_are_checked_on_host(lib):
+    f = lambda x: P(x) if x else None  # noqa: E731
+    # 9000 tokens at V = 131072 need about 18.4 MB > 16 MiB of scratch: refused before any device call
+    st = lib.linear_logp_fwd_noalloc(f(0x1000), f(0x2000), None, f(0x3000), None, 9000, 2688, 131072, -100,
+                                     f(0x4000), f(0x5000), None)
+    assert st == _lib.LLP_ERR_SCRATCH_LIMIT
+    assert lib.linear_logp_fwd_noalloc(None, f(0x2000), None, f(0x3000), None, 4, 64, 100, -100, f(0x4000),
+                                       f(0x5000), None) == _lib.LLP_ERR_NULL_POINTER
+    assert lib.linear_logp_fwd_noalloc(None, None, None, None, None, 0, 64, 100, -100, None, None,
+                                       None) == _lib.LLP_OK
+
+
 def test_python_wrapper_fails_closed_without_gpu():
     import torch
     import lm_head_selected_gb300 as llp
