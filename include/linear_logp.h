@@ -37,7 +37,7 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *     enqueued on it; the library never synchronises.
  *   - Alignment: hidden, weight, grad_hidden, grad_weight and workspace must be
- *     16-byte aligned; bias 16-byte aligned; float arrays 4-byte aligned;
+ *     16-byte aligned; bias and other float arrays 4-byte aligned;
  *     targets 8-byte aligned.
  *   - Shapes: N >= 0, 1 <= D, D % 8 == 0 (16-byte rows for the tensor-memory
  *     copies), 1 <= V, and N, D, V < 2^31 with N*D, V*D and N*V < 2^62.
@@ -171,6 +171,42 @@ int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, cons
                             int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
                             void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/*
+ * Vocab-parallel shards ("Fused Linear LogP", Tensor Parallel Vocab Shards: each
+ * rank holds a contiguous weight shard [V_local, D] starting at global vocab id
+ * vocab_start, computes local online-softmax state, and collectives merge the
+ * global max, sum and target logit; hidden.grad is summed over ranks, the weight
+ * and bias gradients stay local).  The collectives themselves belong to the
+ * caller (e.g. torch.distributed all-gathers); these calls are the device work
+ * around them, and every merge runs in ascending rank order so the results do
+ * not depend on collective timing.
+ *   linear_logp_fwd_shard: per row, the shard's max, its sum of exp(z - max) and
+ *     the target logit if the (global) target lies in this shard, else -inf.
+ *     Workspace: linear_logp_fwd_workspace_bytes(N, D, V_local).
+ *   linear_logp_merge_shards: R shards' triples laid out [R][N] each (rank
+ *     order) -> logp, lse exactly as the unsharded forward defines them; targets
+ *     are valid against global_V.  The shards must partition [0, global_V).
+ *   linear_logp_bwd_shard: with the merged lse, this shard's dz; writes its
+ *     contribution dz_local . W_local to grad_hidden_partial (fp32 [N, D],
+ *     16-byte aligned, may be NULL), and the local grad_weight / grad_bias.
+ *     Workspace: linear_logp_bwd_workspace_bytes(N, D, V_local, has_bias).
+ *   linear_logp_sum_partials: out (bf16, `count` elements) = sum over r = 0..R-1
+ *     in ascending order of parts[r] (fp32, R x count, count % 4 == 0).
+ */
+int linear_logp_fwd_shard(const void* hidden, const void* weight_local, const float* bias_local,
+                          const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V_local,
+                          int64_t vocab_start, int64_t ignore_index, float* out_max, float* out_sumexp,
+                          float* out_target_logit, void* workspace, size_t workspace_bytes, void* stream);
+int linear_logp_merge_shards(const float* shard_max, const float* shard_sumexp, const float* shard_target_logit,
+                             int64_t R, int64_t N, const int64_t* targets, int64_t global_V, int64_t ignore_index,
+                             float* out_logp, float* out_lse, void* stream);
+int linear_logp_bwd_shard(const float* grad_logp, const float* lse, const void* hidden, const void* weight_local,
+                          const float* bias_local, const int64_t* targets, const float* temperature, int64_t N,
+                          int64_t D, int64_t V_local, int64_t vocab_start, int64_t global_V, int64_t ignore_index,
+                          float* grad_hidden_partial, void* grad_weight_local, float* grad_bias_local,
+                          void* workspace, size_t workspace_bytes, void* stream);
+int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* linear_logp_status_string(int status);

@@ -36,6 +36,10 @@ EXPORTED = (
     "linear_logp_bwd_indexed_workspace_bytes",
     "linear_logp_fwd_indexed",
     "linear_logp_bwd_indexed",
+    "linear_logp_fwd_shard",
+    "linear_logp_merge_shards",
+    "linear_logp_bwd_shard",
+    "linear_logp_sum_partials",
 )
 # include/fused_logp.h (logits-input op, same library)
 EXPORTED_FUSED = (
@@ -112,6 +116,16 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_bwd_indexed.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _i64, _p,
                                                 _p, _p, _p, _size, _p]
         lib.linear_logp_bwd_indexed.restype = ctypes.c_int
+        lib.linear_logp_fwd_shard.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p,
+                                              _size, _p]
+        lib.linear_logp_fwd_shard.restype = ctypes.c_int
+        lib.linear_logp_merge_shards.argtypes = [_p, _p, _p, _i64, _i64, _p, _i64, _i64, _p, _p, _p]
+        lib.linear_logp_merge_shards.restype = ctypes.c_int
+        lib.linear_logp_bwd_shard.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p,
+                                              _p, _p, _p, _size, _p]
+        lib.linear_logp_bwd_shard.restype = ctypes.c_int
+        lib.linear_logp_sum_partials.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.linear_logp_sum_partials.restype = ctypes.c_int
         lib.fused_logp_workspace_bytes.argtypes = [_i64, _i64]
         lib.fused_logp_workspace_bytes.restype = _size
         lib.fused_logp_fwd.argtypes = [_p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _p, _p, _p, _size, _p]

@@ -105,7 +105,7 @@ int check_inputs(const void* hidden, const void* weight, const float* bias, cons
   const int s = check_shapes(N, D, V);
   if (s != LLP_OK) return s;
   if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8)) return LLP_ERR_MISALIGNED;
-  if (bias != nullptr && !aligned(bias, 16)) return LLP_ERR_MISALIGNED;
+  if (bias != nullptr && !aligned(bias, 4)) return LLP_ERR_MISALIGNED;
   if (temperature != nullptr && !aligned(temperature, 4)) return LLP_ERR_MISALIGNED;
   return LLP_OK;
 }
@@ -185,7 +185,7 @@ int make_map_part(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
 
 // Output map of a gradient [rows][D] (bf16) or of its segment partials.
 int make_map_grad_out(CUtensorMap* m, const llp::GradGemmParams& p) {
-  if (p.nseg == 1) return make_map(m, p.out, p.D, p.rows, static_cast<uint64_t>(p.D) * 2, 64, 32);
+  if (p.nseg == 1 && !p.f32_out) return make_map(m, p.out, p.D, p.rows, static_cast<uint64_t>(p.D) * 2, 64, 32);
   return make_map_part(m, p.part, p.D, p.rows, p.nseg);
 }
 
@@ -234,9 +234,12 @@ void rec_mark(cudaStream_t s, int id) {
 }
 
 // Forward launch sequence on validated arguments (N > 0, workspace sized by fwd_layout).
+// With sh_max set, `weight` is a vocab shard whose row 0 is global id vocab_start,
+// and the shard's (max, sum, target logit) triple is written instead of logp / lse.
 int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const float* bias, const int64_t* targets,
              const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index, float* out_logp,
-             float* out_lse, uint8_t* ws, cudaStream_t s) {
+             float* out_lse, uint8_t* ws, cudaStream_t s, int64_t vocab_start = 0, float* sh_max = nullptr,
+             float* sh_se = nullptr, float* sh_tl = nullptr) {
   const FwdLayout L = fwd_layout(N, V);
   CUtensorMap tm_h, tm_w;
   if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
@@ -257,22 +260,33 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.part_s = reinterpret_cast<float*>(ws + L.part_s);
   p.zt = reinterpret_cast<float*>(ws + L.zt);
   p.err = dev->status_ptr;
+  p.vocab_start = vocab_start;
+  p.global_V = V;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   rec_mark(s, -1);
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
   rec_mark(s, kKFwdPartials);
-  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (sh_max != nullptr) {
+    if (llp::launch_shard_stats(p, sh_max, sh_se, sh_tl, s) != cudaSuccess) return LLP_ERR_CUDA;
+  } else {
+    if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+  }
   rec_mark(s, kKFwdMerge);
   return LLP_OK;
 }
 
 // Backward launch sequence on validated arguments (N > 0, workspace sized by bwd_layout).
+// For a vocab shard: `weight` starts at global id vocab_start, targets are valid
+// against global_V, and grad_hidden_f32 (fp32 [N, D]) receives this shard's
+// contribution dz_local . W_local instead of a bf16 grad_hidden.
 int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
              const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V,
              int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias, uint8_t* ws,
-             cudaStream_t s) {
+             cudaStream_t s, int64_t vocab_start = 0, int64_t global_V = -1, float* grad_hidden_f32 = nullptr) {
+  if (global_V < 0) global_V = V;
   const bool want_gb = grad_bias != nullptr;
-  const BwdLayout L = bwd_layout(N, D, V, bias != nullptr, grad_hidden != nullptr, grad_weight != nullptr);
+  const bool want_gh = grad_hidden != nullptr || grad_hidden_f32 != nullptr;
+  const BwdLayout L = bwd_layout(N, D, V, bias != nullptr, want_gh, grad_weight != nullptr);
   const int64_t V_pad = static_cast<int64_t>(round_up(static_cast<size_t>(V), 64));
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + L.dz);
 
@@ -298,6 +312,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.dz = dz;
     p.gb_part = want_gb ? reinterpret_cast<float*>(ws + L.gb_part) : nullptr;
     p.err = dev->status_ptr;
+    p.vocab_start = vocab_start;
+    p.global_V = global_V;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
     CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
@@ -307,7 +323,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   }
 
   // B2: grad_hidden = dz . W over fixed vocab segments
-  if (grad_hidden != nullptr) {
+  if (want_gh) {
     CUtensorMap tm_dz, tm_w_mn;
     if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
     if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
@@ -322,6 +338,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.out = static_cast<__nv_bfloat16*>(grad_hidden);
     p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
     p.err = dev->status_ptr;
+    p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
+    if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
     if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;
@@ -329,8 +347,10 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       return LLP_ERR_CUDA;
     rec_mark(s, kKGradHidden);
     if (p.nseg > 1) {
-      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s) != cudaSuccess)
-        return LLP_ERR_CUDA;
+      const cudaError_t e =
+          p.f32_out ? llp::launch_segment_sum_f32(p.part, p.nseg, static_cast<long long>(N) * D, grad_hidden_f32, s)
+                    : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s);
+      if (e != cudaSuccess) return LLP_ERR_CUDA;
       rec_mark(s, kKSegSumHidden);
     }
   }
@@ -350,6 +370,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.kseg_blocks = llp::kKSegment / llp::kTileK;
     p.out = static_cast<__nv_bfloat16*>(grad_weight);
     p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
+    p.f32_out = 0;
     p.err = dev->status_ptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
@@ -606,6 +627,105 @@ int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, cons
 }
 
 // ----------------------------------------------------------------------------
+// Vocab-parallel shards.
+// ----------------------------------------------------------------------------
+int linear_logp_fwd_shard(const void* hidden, const void* weight_local, const float* bias_local,
+                          const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V_local,
+                          int64_t vocab_start, int64_t ignore_index, float* out_max, float* out_sumexp,
+                          float* out_target_logit, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shapes(N, D, V_local);
+  if (st != LLP_OK) return st;
+  if (vocab_start < 0 || vocab_start > kLim31 - V_local) return LLP_ERR_BAD_SHAPE;
+  if (N == 0) return LLP_OK;
+  st = check_inputs(hidden, weight_local, bias_local, targets, temperature, N, D, V_local);
+  if (st != LLP_OK) return st;
+  if (out_max == nullptr || out_sumexp == nullptr || out_target_logit == nullptr || workspace == nullptr)
+    return LLP_ERR_NULL_POINTER;
+  if (!aligned(out_max, 4) || !aligned(out_sumexp, 4) || !aligned(out_target_logit, 4) || !aligned(workspace, 16))
+    return LLP_ERR_MISALIGNED;
+  if (workspace_bytes < fwd_layout(N, V_local).total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+  return fwd_core(dev, hidden, weight_local, bias_local, targets, temperature, N, D, V_local, ignore_index, nullptr,
+                  nullptr, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream), vocab_start, out_max,
+                  out_sumexp, out_target_logit);
+}
+
+int linear_logp_merge_shards(const float* shard_max, const float* shard_sumexp, const float* shard_target_logit,
+                             int64_t R, int64_t N, const int64_t* targets, int64_t global_V, int64_t ignore_index,
+                             float* out_logp, float* out_lse, void* stream) {
+  if (R < 1 || N < 0 || global_V < 1 || N > kLim31 || global_V > kLim31 || !product_ok(R, N) || R * N > kLim62)
+    return LLP_ERR_BAD_SHAPE;
+  if (N == 0) return LLP_OK;
+  if (!shard_max || !shard_sumexp || !shard_target_logit || !targets || !out_logp || !out_lse)
+    return LLP_ERR_NULL_POINTER;
+  if (!aligned(shard_max, 4) || !aligned(shard_sumexp, 4) || !aligned(shard_target_logit, 4) ||
+      !aligned(targets, 8) || !aligned(out_logp, 4) || !aligned(out_lse, 4))
+    return LLP_ERR_MISALIGNED;
+  DeviceInit* dev = nullptr;
+  const int st = init_device(&dev);
+  if (st != LLP_OK) return st;
+  return llp::launch_merge_shards(shard_max, shard_sumexp, shard_target_logit, static_cast<int>(R),
+                                  static_cast<int>(N), reinterpret_cast<const long long*>(targets), global_V,
+                                  ignore_index, out_logp, out_lse, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LLP_OK
+             : LLP_ERR_CUDA;
+}
+
+int linear_logp_bwd_shard(const float* grad_logp, const float* lse, const void* hidden, const void* weight_local,
+                          const float* bias_local, const int64_t* targets, const float* temperature, int64_t N,
+                          int64_t D, int64_t V_local, int64_t vocab_start, int64_t global_V, int64_t ignore_index,
+                          float* grad_hidden_partial, void* grad_weight_local, float* grad_bias_local,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shapes(N, D, V_local);
+  if (st != LLP_OK) return st;
+  if (vocab_start < 0 || global_V < 1 || global_V > kLim31 || vocab_start > global_V - V_local)
+    return LLP_ERR_BAD_SHAPE;
+  if (grad_bias_local != nullptr && bias_local == nullptr) return LLP_ERR_NULL_POINTER;
+  if ((grad_hidden_partial && !aligned(grad_hidden_partial, 16)) ||
+      (grad_weight_local && !aligned(grad_weight_local, 16)) || (grad_bias_local && !aligned(grad_bias_local, 4)))
+    return LLP_ERR_MISALIGNED;
+  if (!grad_hidden_partial && !grad_weight_local && !grad_bias_local) return LLP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInit* dev = nullptr;
+  if (N == 0) {
+    if ((st = init_device(&dev)) != LLP_OK) return st;
+    if (grad_weight_local && cudaMemsetAsync(grad_weight_local, 0, static_cast<size_t>(V_local) * D * 2, s))
+      return LLP_ERR_CUDA;
+    if (grad_bias_local && cudaMemsetAsync(grad_bias_local, 0, static_cast<size_t>(V_local) * 4, s))
+      return LLP_ERR_CUDA;
+    return LLP_OK;
+  }
+  st = check_inputs(hidden, weight_local, bias_local, targets, temperature, N, D, V_local);
+  if (st != LLP_OK) return st;
+  if (grad_logp == nullptr || lse == nullptr || workspace == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(grad_logp, 4) || !aligned(lse, 4) || !aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(N, D, V_local, bias_local != nullptr, grad_hidden_partial != nullptr,
+                                 grad_weight_local != nullptr);
+  if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  if ((st = load_encode_fn()) != LLP_OK) return st;
+  return bwd_core(dev, grad_logp, lse, hidden, weight_local, bias_local, targets, temperature, N, D, V_local,
+                  ignore_index, nullptr, grad_weight_local, grad_bias_local, static_cast<uint8_t*>(workspace), s,
+                  vocab_start, global_V, grad_hidden_partial);
+}
+
+int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream) {
+  if (R < 1 || count < 0 || (count % 4) != 0 || !product_ok(R, count)) return LLP_ERR_BAD_SHAPE;
+  if (count == 0) return LLP_OK;
+  if (parts == nullptr || out_bf16 == nullptr) return LLP_ERR_NULL_POINTER;
+  if (!aligned(parts, 16) || !aligned(out_bf16, 8)) return LLP_ERR_MISALIGNED;
+  DeviceInit* dev = nullptr;
+  const int st = init_device(&dev);
+  if (st != LLP_OK) return st;
+  return llp::launch_segment_sum(parts, static_cast<int>(R), count, static_cast<__nv_bfloat16*>(out_bf16),
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LLP_OK
+             : LLP_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------
 // Logits-input fused log-prob (include/fused_logp.h).
 // ----------------------------------------------------------------------------
 static int fused_check(const void* logits, int dtype, int64_t N, int64_t V, const int64_t* targets) {
@@ -775,6 +895,8 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   p.part_s = reinterpret_cast<float*>(ws + L.part_s);
   p.zt = reinterpret_cast<float*>(ws + L.zt);
   p.err = dev->status_ptr;
+  p.vocab_start = 0;
+  p.global_V = V;
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;

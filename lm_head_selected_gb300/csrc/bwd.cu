@@ -103,10 +103,12 @@ struct DzCfg {
     rs.lse = 0.f;
     rs.t = -1;
     if (rs.n < p.N) {
+      // validity is global; the one-hot column is the target's local id in this
+      // (possibly vocab-sharded) weight, outside [0, V) when another shard holds it
       const long long t = p.targets[rs.n];
-      if (target_ok(t, p.V, p.ignore_index)) {
+      if (target_ok(t, static_cast<int>(p.global_V), p.ignore_index)) {
         rs.valid = true;
-        rs.t = static_cast<int>(t);
+        rs.t = static_cast<int>(t - p.vocab_start);
         if (p.temperature != nullptr) rs.inv_tau = __frcp_rn(p.temperature[rs.n]);
         rs.gs = p.grad_logp[rs.n] * rs.inv_tau;
         rs.lse = p.lse[rs.n];
@@ -118,6 +120,7 @@ struct DzCfg {
                                               uint32_t taddr, RowState& rs, EpiStore& es) {
     const int v0 = ui.n0;
     const bool full = (v0 + BN) <= p.V;
+    const bool bias_vec = full && (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     const int blk = (ui.m0 + row) >> 5;  // 32-row block of this warp
     const int row0 = ui.m0 + row - lane;  // first token row of this warp's slab
 #pragma unroll 1
@@ -130,7 +133,7 @@ struct DzCfg {
         float z[32];
         tmem_load_32cols(taddr + 64 * q + 32 * h, z);
         if (HAS_BIAS) {
-          if (full) {
+          if (bias_vec) {
             const float4* b4 = reinterpret_cast<const float4*>(p.bias + vc);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -227,7 +230,7 @@ struct GradCfg {
     const int seg = u / (p.num_m * p.num_d);
     const int row0 = ui.m0 + row - lane;
     if (row0 >= p.rows) return;  // this warp's rows are all past the end (warp-uniform)
-    if (p.nseg == 1) {
+    if (p.nseg == 1 && !p.f32_out) {
 #pragma unroll 1
       for (int q = 0; q < BN / 64; ++q) {
         const int d0 = ui.n0 + 64 * q;
@@ -285,6 +288,23 @@ __global__ void __launch_bounds__(256) segment_sum_kernel(const float* __restric
   }
 }
 
+// out[i] = sum_{s ascending} part[s][i], kept in fp32.
+__global__ void __launch_bounds__(256) segment_sum_f32_kernel(const float* __restrict__ part, int nseg,
+                                                              long long count, float* __restrict__ out) {
+  const long long n4 = count / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(part)[i];
+    for (int s = 1; s < nseg; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(part + static_cast<size_t>(s) * count)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(out)[i] = acc;
+  }
+}
+
 // grad_bias[v] = sum over 32-row blocks in ascending order.
 __global__ void __launch_bounds__(256) bias_sum_kernel(const float* __restrict__ gb_part, int nblocks, int V,
                                                        float* __restrict__ out) {
@@ -332,6 +352,15 @@ cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __n
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
   segment_sum_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, cudaStream_t s) {
+  const int threads = 256;
+  long long blocks = (count / 4 + threads - 1) / threads;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  segment_sum_f32_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
   return cudaGetLastError();
 }
 

@@ -80,8 +80,10 @@ struct FwdCfg {
     rs.inv_tau = 1.f;
     rs.tloc = -1;
     if (rs.n < p.N) {
+      // local vocab id of the target (this weight may be a vocab shard starting at vocab_start)
       const long long t = p.targets[rs.n];
-      if (target_valid(t, p.V, p.ignore_index)) rs.tloc = static_cast<int>(t - ui.n0);
+      const long long tl = t - p.vocab_start;
+      if (t != p.ignore_index && tl >= 0 && tl < static_cast<long long>(p.V)) rs.tloc = static_cast<int>(tl - ui.n0);
       if (p.temperature != nullptr) rs.inv_tau = __frcp_rn(p.temperature[rs.n]);
     }
   }
@@ -90,6 +92,8 @@ struct FwdCfg {
                                               uint32_t taddr, RowState& rs, EpiStore&) {
     const int v0 = ui.n0 + j * BN;
     const bool full = (v0 + BN) <= p.V;
+    // a bias slice (a vocab shard's) may start at any float: vector loads only when 16-byte aligned
+    const bool bias_vec = full && (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     const int tl = rs.tloc - j * BN;
     const bool mine = (tl >= 0) && (tl < BN);
     const bool any_t = __any_sync(0xffffffffu, mine);
@@ -99,7 +103,7 @@ struct FwdCfg {
       tmem_load_32cols(taddr + c * 32, z);
       const int vc = v0 + c * 32;
       if (HAS_BIAS) {
-        if (full) {
+        if (bias_vec) {
           const float4* b4 = reinterpret_cast<const float4*>(p.bias + vc);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -170,6 +174,75 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __re
   const float ls = logf(S);
   out_lse[n] = M + ls;
   out_logp[n] = (p.zt[n] - M) - ls;
+}
+
+// Vocab-parallel shard statistics ("Fused Linear LogP", Tensor Parallel Vocab
+// Shards: each rank computes local online-softmax state that collectives then
+// merge): per row the shard's max, its sum of exp(z - max) (splits merged in
+// ascending order) and the target logit when the target lies in the shard,
+// else -inf.
+__global__ void __launch_bounds__(256) shard_stats_kernel(FwdParams p, float* __restrict__ out_max,
+                                                          float* __restrict__ out_se, float* __restrict__ out_tl) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= p.N) return;
+  float M = -INFINITY;
+  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, p.part_m[static_cast<size_t>(s) * p.N + n]);
+  float S = 0.f;
+  for (int s = 0; s < p.num_splits; ++s) {
+    const size_t i = static_cast<size_t>(s) * p.N + n;
+    S += p.part_s[i] * exp2f((p.part_m[i] - M) * kLog2e);
+  }
+  const long long t = p.targets[n];
+  const long long tl = t - p.vocab_start;
+  const bool local = t != p.ignore_index && tl >= 0 && tl < static_cast<long long>(p.V);
+  out_max[n] = M;
+  out_se[n] = S;
+  out_tl[n] = local ? p.zt[n] : -INFINITY;
+}
+
+// Merge of R shards' (max, sum, target logit) in ascending rank order, then the
+// same final expression as the unsharded merge.  Exactly one shard holds a
+// valid target, so the target logit is the largest of the R entries.
+__global__ void __launch_bounds__(256) merge_shards_kernel(const float* __restrict__ mx, const float* __restrict__ se,
+                                                           const float* __restrict__ tl, int R, int N,
+                                                           const long long* __restrict__ targets, long long global_V,
+                                                           long long ignore_index, float* __restrict__ out_logp,
+                                                           float* __restrict__ out_lse) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const long long t = targets[n];
+  if (t == ignore_index || t < 0 || t >= global_V) {
+    out_logp[n] = 0.f;
+    out_lse[n] = -INFINITY;
+    return;
+  }
+  float M = -INFINITY, zt = -INFINITY;
+  for (int r = 0; r < R; ++r) {
+    M = fmaxf(M, mx[static_cast<size_t>(r) * N + n]);
+    zt = fmaxf(zt, tl[static_cast<size_t>(r) * N + n]);
+  }
+  float S = 0.f;
+  for (int r = 0; r < R; ++r) {
+    const size_t i = static_cast<size_t>(r) * N + n;
+    S += se[i] * exp2f((mx[i] - M) * kLog2e);
+  }
+  const float ls = logf(S);
+  out_lse[n] = M + ls;
+  out_logp[n] = (zt - M) - ls;
+}
+
+cudaError_t launch_shard_stats(const FwdParams& p, float* out_max, float* out_sumexp, float* out_tlogit,
+                               cudaStream_t s) {
+  shard_stats_kernel<<<(p.N + 255) / 256, 256, 0, s>>>(p, out_max, out_sumexp, out_tlogit);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_shards(const float* mx, const float* se, const float* tl, int R, int N,
+                                const long long* targets, long long global_V, long long ignore_index, float* out_logp,
+                                float* out_lse, cudaStream_t s) {
+  merge_shards_kernel<<<(N + 255) / 256, 256, 0, s>>>(mx, se, tl, R, N, targets, global_V, ignore_index, out_logp,
+                                                      out_lse);
+  return cudaGetLastError();
 }
 
 cudaError_t fwd_setup(LaunchCaps* caps) {

@@ -50,6 +50,8 @@ struct FwdParams {
   float* part_s;   // [num_splits][N] sum of exp(z - part_m) over the split
   float* zt;       // [N] target logit (written by the split that holds the target)
   unsigned int* err;
+  long long vocab_start;  // global id of local vocab row 0 (vocab-parallel shards; 0 otherwise)
+  long long global_V;     // global vocab size (== V unless sharded)
 };
 
 struct DzParams {
@@ -64,6 +66,8 @@ struct DzParams {
   __nv_bfloat16* dz;  // [N][V_pad]
   float* gb_part;     // [num_m*4][V]: per 32-row block column sums of dz (bias only)
   unsigned int* err;
+  long long vocab_start;  // global id of local vocab row 0 (vocab-parallel shards; 0 otherwise)
+  long long global_V;     // global vocab size: decides which targets are valid
 };
 
 struct GradGemmParams {
@@ -71,9 +75,10 @@ struct GradGemmParams {
   int D;             // output columns
   int K;             // reduction extent: V for grad_hidden, N for grad_weight
   int num_m, num_d, nseg, kseg_blocks;
-  __nv_bfloat16* out;  // [rows][D] bf16 when nseg == 1
-  float* part;         // [nseg][rows][D] fp32 partials when nseg > 1
+  __nv_bfloat16* out;  // [rows][D] bf16 when nseg == 1 and !f32_out
+  float* part;         // [nseg][rows][D] fp32 partials when nseg > 1 or f32_out
   unsigned int* err;
+  int f32_out;         // 1: always write fp32 partials (a vocab shard's grad_hidden contribution)
 };
 
 // Launchers (return the launch error, never synchronise).  `units` is the
@@ -82,6 +87,14 @@ cudaError_t fwd_setup(LaunchCaps* caps);
 cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,
                                 long long units, const LaunchCaps& caps, cudaStream_t s);
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s);
+// Vocab-parallel shards: per-row (max, sum of exp(z - max), target logit or -inf)
+// of this shard, and the ascending-rank merge of R shards' triples.
+cudaError_t launch_shard_stats(const FwdParams& p, float* out_max, float* out_sumexp, float* out_tlogit,
+                               cudaStream_t s);
+cudaError_t launch_merge_shards(const float* mx, const float* se, const float* tl, int R, int N,
+                                const long long* targets, long long global_V, long long ignore_index, float* out_logp,
+                                float* out_lse, cudaStream_t s);
+cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, cudaStream_t s);
 
 cudaError_t bwd_setup(LaunchCaps* caps);
 // The third tensor map is the output the epilogue stores through: dz (bf16,

@@ -46,6 +46,29 @@ struct Vec<kDtypeBF16> {
     }
   }
   static __device__ __forceinline__ float load1(const T* p) { return __bfloat162float(*p); }
+  // The W elements at p as stored, elements at or past n_valid reading as -inf.
+  // One 16-byte load only when `vec` (p is 16-byte aligned) and all W are valid;
+  // otherwise element-wise 2-byte loads.
+  static __device__ __forceinline__ uint4 load_raw(const T* p, int n_valid, bool vec) {
+    if (vec && n_valid >= W) return __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t w[4];
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (2 * i < n_valid) ? q[2 * i] : 0xFF80u;
+      const uint32_t hi = (2 * i + 1 < n_valid) ? q[2 * i + 1] : 0xFF80u;
+      w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  static __device__ __forceinline__ void unpack(const uint4& r, float (&v)[W]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
   static __device__ __forceinline__ void store(T* p, const float (&v)[W]) {
     uint4 r;
     __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]),
@@ -70,6 +93,18 @@ struct Vec<kDtypeF32> {
     v[3] = r.w;
   }
   static __device__ __forceinline__ float load1(const T* p) { return __ldg(p); }
+  static __device__ __forceinline__ uint4 load_raw(const T* p, int n_valid, bool vec) {
+    if (vec && n_valid >= W) return __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t ninf = __float_as_uint(-INFINITY);
+    return make_uint4(n_valid > 0 ? __float_as_uint(p[0]) : ninf, n_valid > 1 ? __float_as_uint(p[1]) : ninf,
+                      n_valid > 2 ? __float_as_uint(p[2]) : ninf, n_valid > 3 ? __float_as_uint(p[3]) : ninf);
+  }
+  static __device__ __forceinline__ void unpack(const uint4& r, float (&v)[W]) {
+    v[0] = __uint_as_float(r.x);
+    v[1] = __uint_as_float(r.y);
+    v[2] = __uint_as_float(r.z);
+    v[3] = __uint_as_float(r.w);
+  }
   static __device__ __forceinline__ void store(T* p, const float (&v)[W]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
@@ -110,42 +145,52 @@ __device__ __forceinline__ void block_merge(float& m, float& s, float* sm_m, flo
   s = sm_s[0];
 }
 
-// Each thread owns elements [split0 + (it * kLThreads + tid) * W, + W) for it = 0..ITERS-1.
+// Each thread owns elements [split0 + (it * kLThreads + tid) * W, + W) for it = 0..ITERS-1,
+// loaded 8 vectors at a time and kept packed until they are folded into the
+// thread's (max, sum) pair, so few registers are live and several CTAs per SM
+// keep many loads in flight.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kLThreads) logits_split_kernel(const typename Vec<DT>::T* __restrict__ z, int N,
-                                                                 int V, int S, float* __restrict__ part_m,
-                                                                 float* __restrict__ part_s) {
+__global__ void __launch_bounds__(kLThreads, 3) logits_split_kernel(const typename Vec<DT>::T* __restrict__ z,
+                                                                    int N, int V, int S, float* __restrict__ part_m,
+                                                                    float* __restrict__ part_s) {
   using VV = Vec<DT>;
   constexpr int W = VV::W;
   constexpr int ITERS = kLogitsSplit / (kLThreads * W);
+  constexpr int CHUNK = ITERS < 8 ? ITERS : 8;
   __shared__ float sm_m[kLThreads / 32], sm_s[kLThreads / 32];
   const long long cta = blockIdx.x;
   const int row = static_cast<int>(cta / S);
   const int split = static_cast<int>(cta - static_cast<long long>(row) * S);
   const int v0 = split * kLogitsSplit;
   const typename VV::T* zr = z + static_cast<size_t>(row) * V;
-  float vals[ITERS][W];
+  float m = -INFINITY, s = 0.f;
 #pragma unroll
-  for (int it = 0; it < ITERS; ++it) {
-    const int v = v0 + (it * kLThreads + threadIdx.x) * W;
-    if (VEC && v + W <= V) {
-      VV::load(zr + v, vals[it]);
-    } else {
+  for (int c0 = 0; c0 < ITERS; c0 += CHUNK) {
+    uint4 raw[CHUNK];
 #pragma unroll
-      for (int k = 0; k < W; ++k) vals[it][k] = (v + k < V) ? VV::load1(zr + v + k) : -INFINITY;
+    for (int i = 0; i < CHUNK; ++i) {
+      const int v = v0 + ((c0 + i) * kLThreads + threadIdx.x) * W;
+      // n_valid <= 0: nothing is read and every element is -inf
+      raw[i] = VV::load_raw(zr + (v < V ? v : 0), V - v, VEC);
     }
-  }
-  float m = -INFINITY;
+    float cm = -INFINITY;
 #pragma unroll
-  for (int it = 0; it < ITERS; ++it)
+    for (int i = 0; i < CHUNK; ++i) {
+      float x[W];
+      VV::unpack(raw[i], x);
 #pragma unroll
-    for (int k = 0; k < W; ++k) m = fmaxf(m, vals[it][k]);
-  float s = 0.f;
-  if (m != -INFINITY) {
+      for (int k = 0; k < W; ++k) cm = fmaxf(cm, x[k]);
+    }
+    if (cm == -INFINITY) continue;
+    float cs = 0.f;
 #pragma unroll
-    for (int it = 0; it < ITERS; ++it)
+    for (int i = 0; i < CHUNK; ++i) {
+      float x[W];
+      VV::unpack(raw[i], x);
 #pragma unroll
-      for (int k = 0; k < W; ++k) s += exp2f((vals[it][k] - m) * kLog2eL);
+      for (int k = 0; k < W; ++k) cs += exp2f((x[k] - cm) * kLog2eL);
+    }
+    merge_ms(m, s, cm, cs);
   }
   block_merge(m, s, sm_m, sm_s);
   if (threadIdx.x == 0) {

@@ -90,7 +90,7 @@ def test_fwd_rejects_bad_arguments_on_host(lib):
     assert _fwd(lib, hidden=0x1008) == _lib.LLP_ERR_MISALIGNED
     assert _fwd(lib, weight=0x2004) == _lib.LLP_ERR_MISALIGNED
     assert _fwd(lib, targets=0x3004) == _lib.LLP_ERR_MISALIGNED
-    assert _fwd(lib, bias=0x7008) == _lib.LLP_ERR_MISALIGNED
+    assert _fwd(lib, bias=0x7002) == _lib.LLP_ERR_MISALIGNED
     assert _fwd(lib, temp=0x7002) == _lib.LLP_ERR_MISALIGNED
     assert _fwd(lib, ws=0x6008) == _lib.LLP_ERR_MISALIGNED
     need = lib.linear_logp_fwd_workspace_bytes(4, 64, 100)

@@ -150,3 +150,19 @@ def test_autograd_leading_shape():
     assert torch.equal(h.grad.reshape(300, 128), gh)
     assert torch.equal(w.grad, gw)
     assert torch.equal(b.grad, gb)
+
+
+def test_bias_at_unaligned_offset():
+    """A bias that starts one float into its buffer (a vocab shard's slice): scalar bias loads, same results."""
+    inp = workloads.make_inputs(150, 128, 1300, seed=21, weight_std=0.2, bias_std=0.4, n_ignore=2, grad_std=1.0)
+    d = to_device(inp)
+    buf = torch.zeros(inp.V + 1, dtype=torch.float32, device=d["bias"].device)
+    buf[1:] = d["bias"]
+    d["bias"] = buf[1:]
+    assert d["bias"].data_ptr() % 16 != 0
+    logp, lse = gpu_fwd(d)
+    check_device_status()
+    check_forward(inp, logp, lse)
+    gh, gw, gb = gpu_bwd(d, lse)
+    check_device_status()
+    check_backward(inp, gh, gw, gb)
