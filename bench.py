@@ -54,9 +54,15 @@ WORKLOADS = {
 PAGES_TOKENS_PER_S = 16384 / 0.3512
 PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (context: other hardware)"
 
-# DRAM traffic per launch of the dominant kernel from one ncu capture, valid only
-# while the kernel sources are unchanged (checked by hash).  None until captured.
-NCU_TRAFFIC = None  # e.g. {"kernel": "grad_hidden", "bytes_per_launch": ..., "sources_sha": "..."}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# tcgen05 GEMM kernel from one single-pass ncu capture of the default workload,
+# valid only while the kernel sources are unchanged (checked by hash).
+NCU_TRAFFIC = {
+    "workload": "rl_head_fwd_bwd",
+    "sources_sha": "1387fde1b13c3a45",
+    "bytes_per_launch": {"fwd_partials": 1731198208 + 37129728, "dlogits": 4687911424 + 4275526400,
+                         "grad_hidden": 18181482240 + 701606656, "grad_weight": 13261341696 + 699959552},
+}
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
 
@@ -341,8 +347,12 @@ def run_ours(args):
                 "algorithmic_per_launch": f"{dk['algorithmic_gb'] * 1e9:.4e} bytes (every operand read once, "
                                           f"every result written once)"}
     roof["traffic"] = None
-    if NCU_TRAFFIC and NCU_TRAFFIC.get("kernel") == dom and NCU_TRAFFIC.get("sources_sha") == sources_sha():
-        roof["traffic"] = NCU_TRAFFIC["bytes_per_launch"]
+    if (NCU_TRAFFIC and NCU_TRAFFIC["workload"] == args.workload and NCU_TRAFFIC["sources_sha"] == sources_sha()
+            and dom in NCU_TRAFFIC["bytes_per_launch"]):
+        roof["traffic"] = NCU_TRAFFIC["bytes_per_launch"][dom]
+        for k, v in NCU_TRAFFIC["bytes_per_launch"].items():
+            if k in kernels:
+                kernels[k]["dram_gb_ncu"] = v / 1e9
 
     # forward-only throughput (same inputs), for context
     barrier()

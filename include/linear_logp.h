@@ -75,9 +75,11 @@ enum {
  * and the captured target logits. */
 size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V);
 
-/* Bytes of workspace linear_logp_bwd needs: the bf16 dlogits buffer
- * [N, round_up(V, 64)], the grad_bias partials when has_bias != 0, and the fp32
- * K-segment partials of grad_hidden (V > 32768) and grad_weight (N > 32768). */
+/* Bytes of workspace linear_logp_bwd needs: two work-ticket counters of the
+ * gradient GEMMs (set by the library itself; the workspace need not be
+ * zeroed), the bf16 dlogits buffer [N, round_up(V, 64)], the grad_bias
+ * partials when has_bias != 0, and the fp32 K-segment partials of grad_hidden
+ * (V > 32768) and grad_weight (N > 32768). */
 size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_bias);
 
 /*
@@ -242,7 +244,11 @@ int linear_logp_selftest_wait_timeout(unsigned long long limit_ns, void* stream)
 /* Synchronises `stream`, then reads and clears the current device's kernel
  * status word.  Returns LLP_OK if no kernel gave up on a wait since the last
  * call, LLP_ERR_DEVICE_TIMEOUT if one did (the detailed code goes to
- * *device_code when it is not NULL), or LLP_ERR_CUDA. */
+ * *device_code when it is not NULL), or LLP_ERR_CUDA.  Detailed codes: 1 a
+ * tensor-core issuer waited for an operand stage, 2 a loader waited for a free
+ * stage, 3 an epilogue waited for an accumulator, 4 the issuer waited for a
+ * drained accumulator, 5 in-flight tensor-core work did not finish at
+ * teardown, 6 the self-test below, 7 a role waited for its next work-unit id. */
 int linear_logp_device_status(void* stream, unsigned int* device_code);
 
 #ifdef __cplusplus

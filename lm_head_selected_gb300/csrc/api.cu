@@ -136,7 +136,7 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 }
 
 struct BwdLayout {
-  size_t dz, gb_part, dh_part, dw_part, total;
+  size_t sched, dz, gb_part, dh_part, dw_part, total;
   bool has_gb, has_dh, has_dw;
 };
 
@@ -147,6 +147,7 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, b
   const size_t nseg_n = static_cast<size_t>(cdiv(N, llp::kKSegment));
   Carver c;
   BwdLayout L;
+  L.sched = c.take(llp::kNumSchedCounters * sizeof(int));
   L.dz = c.take(static_cast<size_t>(N) * V_pad * 2);
   L.has_gb = bias;
   L.gb_part = bias ? c.take(num_m * (llp::kUnitM / 32) * static_cast<size_t>(V) * sizeof(float)) : 0;
@@ -289,6 +290,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   const BwdLayout L = bwd_layout(N, D, V, bias != nullptr, want_gh, grad_weight != nullptr);
   const int64_t V_pad = static_cast<int64_t>(round_up(static_cast<size_t>(V), 64));
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + L.dz);
+  int* sched = reinterpret_cast<int*>(ws + L.sched);  // zeroed by the dlogits kernel
 
   // B1: dlogits (+ grad_bias partials)
   {
@@ -314,6 +316,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.err = dev->status_ptr;
     p.vocab_start = vocab_start;
     p.global_V = global_V;
+    p.sched_reset = sched;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
     CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
@@ -339,6 +342,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
     p.err = dev->status_ptr;
     p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
+    p.sched = sched + 0;
     if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
@@ -372,6 +376,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
     p.f32_out = 0;
     p.err = dev->status_ptr;
+    p.sched = sched + 1;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
     if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;

@@ -76,6 +76,13 @@ struct DzCfg {
 
   static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_last(); }
   static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+  static constexpr bool DYNAMIC = false;
+  static __device__ __forceinline__ int* sched_counter(const Params&) { return nullptr; }
+  // the gradient GEMMs that follow on the stream start from ticket 0
+  static __device__ __forceinline__ void on_launch(const Params& p) {
+    if (p.sched_reset != nullptr)
+      for (int i = 0; i < kNumSchedCounters; ++i) p.sched_reset[i] = 0;
+  }
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.num_m * p.num_vt; }
 
@@ -92,6 +99,7 @@ struct DzCfg {
     ui.ntiles = 1;
     ui.kb0 = 0;
     ui.nkb = (p.D + BK - 1) / BK;
+    ui.bn = BN;
     return ui;
   }
 
@@ -184,6 +192,7 @@ template <bool A_MN_, bool B_MN_>
 struct GradCfg {
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
+  static_assert(B_MN, "half-width column tiles load B in 64-row MN-major boxes");
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
   static constexpr int STAGES = PAIR ? kPairStages : 4;
@@ -197,6 +206,11 @@ struct GradCfg {
 
   static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_normal(); }
   static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+  // units are claimed in ascending order from a ticket counter, so the tiles
+  // that share A rows or a K window of B run together
+  static constexpr bool DYNAMIC = (LLP_DYNAMIC_SCHED & (A_MN ? 2 : 1)) != 0;
+  static __device__ __forceinline__ int* sched_counter(const Params& p) { return p.sched; }
+  static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.nseg * p.num_m * p.num_d; }
 
@@ -215,6 +229,7 @@ struct GradCfg {
     ui.ntiles = 1;
     ui.kb0 = seg * p.kseg_blocks;
     ui.nkb = min(p.kseg_blocks, total_kb - ui.kb0);
+    ui.bn = (LLP_HALF_TILE && p.D - ui.n0 <= BN / 2) ? BN / 2 : BN;  // ragged last column tile: half-width MMA
     return ui;
   }
 

@@ -51,6 +51,9 @@ struct FwdCfg {
 
   static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_last(); }
   static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+  static constexpr bool DYNAMIC = false;
+  static __device__ __forceinline__ int* sched_counter(const Params&) { return nullptr; }
+  static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.num_m * p.num_splits; }
 
@@ -69,6 +72,7 @@ struct FwdCfg {
     ui.ntiles = min(TPS, p.num_vt - split * TPS);
     ui.kb0 = 0;
     ui.nkb = (p.D + BK - 1) / BK;
+    ui.bn = BN;
     return ui;
   }
 

@@ -21,10 +21,20 @@
 //
 // A unit of work is a run of `ntiles` consecutive output tiles that share A
 // rows (the forward's vocab split) or a single tile with a K range (a fixed K
-// segment of the gradient GEMMs).  CTAs (or pairs) take units round-robin;
-// which one runs a unit never changes any arithmetic, so results do not depend
-// on the grid size, and every per-row / per-element reduction runs in a fixed
-// order.
+// segment of the gradient GEMMs).  CTAs (or pairs) take units either
+// round-robin (static) or, for configurations with DYNAMIC set, in ascending
+// order from a global ticket counter: the pair's producer draws the ticket and
+// hands the unit id to every other role through a small ring of slots in
+// shared memory.  In-order claiming keeps the units that share operands
+// running at the same time, so their operands are re-used from L2 instead of
+// drifting apart over the launch.  Which CTA runs a unit never changes any
+// arithmetic, so results do not depend on the grid size or on the schedule,
+// and every per-row / per-element reduction runs in a fixed order.
+//
+// A unit's tiles are BN wide, or BN/2 (`UnitInfo::bn`, MN-major B only) for a
+// last column tile with no more than BN/2 columns when LLP_HALF_TILE is set.
+// It is off by default: the half-width MMA halves the compute per stage while
+// the copy latency stays, and the stalls cost more than the padding saves.
 //
 // Operand layouts (both 128-byte swizzled, as TMA writes them):
 //   K-major  : box {64 K, R rows}; row pitch 128 B; 8-row groups 1024 B apart.
@@ -49,7 +59,10 @@ struct UnitInfo {
   int ntiles;  // tiles along N, each BN wide
   int kb0;     // first k-block (BK elements each)
   int nkb;     // k-blocks per tile
+  int bn;      // MMA N of the unit's tiles: Cfg::BN, or Cfg::BN / 2 for a ragged last column tile
 };
+
+constexpr int kSchedDepth = 4;  // unit-id slots between the ticket drawer and the other roles
 
 template <class Cfg>
 struct Plan {
@@ -66,6 +79,10 @@ struct Plan {
   static constexpr int BAR_BYTES = 256;
   static constexpr int TOTAL = BAR_OFFSET + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int EPI_ARRIVALS = 4 * NCTA;                // one per epilogue warp of the pair
+  // readers of a unit-id slot: MMA lane + 4 epilogue warps (+ the odd CTA's producer and 4 epilogue warps)
+  static constexpr int SCHED_READERS = PAIR ? 10 : 5;
+  static constexpr int BAR_USED = (2 * Cfg::STAGES + 5 + 2 * kSchedDepth) * 8 + 8 + 4 * kSchedDepth;
+  static_assert(BAR_USED <= BAR_BYTES, "barrier region overflow");
   static_assert(TOTAL <= 232448, "shared memory budget exceeded");
   static_assert(B_ROWS % 64 == 0 && B_ROWS <= 256, "B half must be whole 64-row swizzle atoms");
 };
@@ -76,6 +93,9 @@ struct SharedState {
   uint64_t* tmem_full;
   uint64_t* tmem_empty;
   uint64_t* drain;
+  uint64_t* sched_full;   // [kSchedDepth], this CTA: a unit id is in the slot
+  uint64_t* sched_empty;  // [kSchedDepth], even CTA: every reader has taken the slot
+  int* sched_slot;        // [kSchedDepth], this CTA
   volatile int* abort;
   unsigned int* err;
   uint8_t* tiles;
@@ -138,6 +158,52 @@ __device__ __forceinline__ void epi_slab_store_3d(EpiStore& es, uint32_t buf, in
 }
 
 // ----------------------------------------------------------------------------
+// Unit schedule.  The k-th unit of this CTA (pair) is >= 0 a unit id, -1 no
+// more units, -2 a wait gave up (the caller returns).
+// ----------------------------------------------------------------------------
+// Even CTA's producer: publish unit `u` (or -1) as this pair's k-th unit.
+template <class Cfg>
+__device__ __forceinline__ int publish_unit(const SharedState& st, int k, int u) {
+  const int s = k % kSchedDepth;
+  const uint32_t ph = static_cast<uint32_t>(k / kSchedDepth) & 1u;
+  if (!mbar_wait_cluster(&st.sched_empty[s], ph ^ 1u, st.abort, st.err, kDevTimeoutSched)) return -2;
+  st.sched_slot[s] = u;
+  mbar_arrive(&st.sched_full[s]);
+  if (Plan<Cfg>::PAIR) {
+    st_shared_cluster_u32(map_to_cta(smem_u32(&st.sched_slot[s]), 1), static_cast<uint32_t>(u));
+    mbar_arrive_cluster(map_to_cta(smem_u32(&st.sched_full[s]), 1));  // release: orders the store above
+  }
+  return u;
+}
+
+// Any other role: take the k-th unit id from this CTA's slot and release the slot.
+// With warp_wide, every lane of the warp calls it: lane 0 waits, reads and
+// releases, and the id reaches the other lanes by shuffle.
+template <class Cfg>
+__device__ __forceinline__ int receive_unit(const SharedState& st, int k, bool warp_wide) {
+  int u = -2;
+  if (!warp_wide || (threadIdx.x & 31) == 0) {
+    const int s = k % kSchedDepth;
+    const uint32_t ph = static_cast<uint32_t>(k / kSchedDepth) & 1u;
+    if (mbar_wait_cluster(&st.sched_full[s], ph, st.abort, st.err, kDevTimeoutSched)) {
+      u = *reinterpret_cast<volatile int*>(&st.sched_slot[s]);
+      if (Plan<Cfg>::PAIR)
+        mbar_arrive_cluster(map_to_cta(smem_u32(&st.sched_empty[s]), 0));
+      else
+        mbar_arrive(&st.sched_empty[s]);
+    }
+  }
+  if (warp_wide) u = __shfl_sync(0xffffffffu, u, 0);
+  return u;
+}
+
+template <class Cfg>
+__device__ __forceinline__ int static_unit(const SharedState& st, const typename Cfg::Params& p, int k) {
+  const int u = st.unit_first + k * st.unit_stride;
+  return u < Cfg::num_units(p) ? u : -1;
+}
+
+// ----------------------------------------------------------------------------
 // Producer: one lane of warp 0 in every CTA.
 // ----------------------------------------------------------------------------
 template <class Cfg>
@@ -150,18 +216,37 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
   int stage = 0;
   uint32_t phase = 0;
   const int num_units = Cfg::num_units(p);
-  for (int u = st.unit_first; u < num_units; u += st.unit_stride) {
+  int ticket = 0;
+  if constexpr (Cfg::DYNAMIC) {
+    if (leader) ticket = atomicAdd(Cfg::sched_counter(p), 1);
+  }
+  for (int k = 0;; ++k) {
+    int u;
+    if constexpr (Cfg::DYNAMIC)
+      u = leader ? publish_unit<Cfg>(st, k, ticket < num_units ? ticket : -1) : receive_unit<Cfg>(st, k, false);
+    else
+      u = static_unit<Cfg>(st, p, k);
+    if (u < 0) return;
     const UnitInfo ui = Cfg::unit(p, u);
     const int a_row = ui.m0 + static_cast<int>(st.rank) * BM;
+    // B rows this CTA loads per k-block: half of the unit's N in pair mode
+    const int b_rows = P::PAIR ? ui.bn / 2 : ui.bn;
+    const uint32_t tx = static_cast<uint32_t>(P::NCTA * (P::A_BYTES + b_rows * BK * 2));
     for (int j = 0; j < ui.ntiles; ++j) {
-      const int b_row = ui.n0 + j * Cfg::BN + static_cast<int>(st.rank) * P::B_ROWS;
+      const int b_row = ui.n0 + j * Cfg::BN + static_cast<int>(st.rank) * b_rows;
       for (int kb = 0; kb < ui.nkb; ++kb) {
+        if constexpr (Cfg::DYNAMIC) {
+          // draw the next ticket a few k-blocks before the unit ends, so its
+          // latency hides behind the loads still to issue
+          if (leader && j == ui.ntiles - 1 && kb == (ui.nkb > 4 ? ui.nkb - 4 : 0))
+            ticket = atomicAdd(Cfg::sched_counter(p), 1);
+        }
         if (!mbar_wait(&st.empty[stage], phase ^ 1u, st.abort, st.err, kDevTimeoutEmpty)) return;
         const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
         const uint32_t sB = sA + P::A_BYTES;
         const int kx = (ui.kb0 + kb) * BK;
         if (P::PAIR) {
-          if (leader) mbar_arrive_expect_tx(&st.full[stage], P::TX_BYTES);
+          if (leader) mbar_arrive_expect_tx(&st.full[stage], tx);
           const uint32_t bar = map_to_cta(smem_u32(&st.full[stage]), 0);
           if (!Cfg::A_MN) {
             tma_load_2d_pair(sA, tmA, bar, kx, a_row, polA);
@@ -172,12 +257,10 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
           if (!Cfg::B_MN) {
             tma_load_2d_pair(sB, tmB, bar, kx, b_row, polB);
           } else {
-#pragma unroll
-            for (int i = 0; i < P::B_ROWS / 64; ++i)
-              tma_load_2d_pair(sB + i * 8192, tmB, bar, b_row + 64 * i, kx, polB);
+            for (int i = 0; i < b_rows / 64; ++i) tma_load_2d_pair(sB + i * 8192, tmB, bar, b_row + 64 * i, kx, polB);
           }
         } else {
-          mbar_arrive_expect_tx(&st.full[stage], P::TX_BYTES);
+          mbar_arrive_expect_tx(&st.full[stage], tx);
           if (!Cfg::A_MN) {
             tma_load_2d(sA, tmA, &st.full[stage], kx, a_row, polA);
           } else {
@@ -188,8 +271,7 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
           if (!Cfg::B_MN) {
             tma_load_2d(sB, tmB, &st.full[stage], kx, b_row, polB);
           } else {
-#pragma unroll
-            for (int i = 0; i < P::B_ROWS / 64; ++i)
+            for (int i = 0; i < b_rows / 64; ++i)
               tma_load_2d(sB + i * 8192, tmB, &st.full[stage], b_row + 64 * i, kx, polB);
           }
         }
@@ -216,13 +298,20 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 template <class Cfg>
 __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
   using P = Plan<Cfg>;
-  constexpr uint32_t idesc = make_idesc_bf16_f32(P::UM, Cfg::BN, Cfg::A_MN, Cfg::B_MN);
+  constexpr uint32_t idesc_full = make_idesc_bf16_f32(P::UM, Cfg::BN, Cfg::A_MN, Cfg::B_MN);
+  constexpr uint32_t idesc_half = make_idesc_bf16_f32(P::UM, Cfg::BN / 2, Cfg::A_MN, Cfg::B_MN);
   int stage = 0;
   uint32_t phase = 0;
   uint32_t acc_i = 0;
-  const int num_units = Cfg::num_units(p);
-  for (int u = st.unit_first; u < num_units; u += st.unit_stride) {
+  for (int k = 0;; ++k) {
+    int u;
+    if constexpr (Cfg::DYNAMIC)
+      u = receive_unit<Cfg>(st, k, false);
+    else
+      u = static_unit<Cfg>(st, p, k);
+    if (u < 0) return;
     const UnitInfo ui = Cfg::unit(p, u);
+    const uint32_t idesc = ui.bn == Cfg::BN ? idesc_full : idesc_half;
     for (int j = 0; j < ui.ntiles; ++j, ++acc_i) {
       const uint32_t buf = acc_i & 1u;
       const uint32_t acc_phase = (acc_i >> 1) & 1u;
@@ -281,8 +370,13 @@ __device__ __forceinline__ void run_epilogue(const SharedState& st, const CUtens
   es.lane = lane;
   uint32_t acc_i = 0;
   bool ok = true;
-  const int num_units = Cfg::num_units(p);
-  for (int u = st.unit_first; ok && u < num_units; u += st.unit_stride) {
+  for (int k = 0; ok; ++k) {
+    int u;
+    if constexpr (Cfg::DYNAMIC)
+      u = receive_unit<Cfg>(st, k, true);
+    else
+      u = static_unit<Cfg>(st, p, k);
+    if (u < 0) break;
     const UnitInfo ui = Cfg::unit(p, u);
     typename Cfg::RowState rs;
     Cfg::unit_begin(p, ui, u, row, rs);
@@ -328,8 +422,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   st.tmem_full = st.empty + Cfg::STAGES;
   st.tmem_empty = st.tmem_full + 2;
   st.drain = st.tmem_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(st.drain + 1);
+  st.sched_full = st.drain + 1;
+  st.sched_empty = st.sched_full + kSchedDepth;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(st.sched_empty + kSchedDepth);
   st.abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  st.sched_slot = reinterpret_cast<int*>(tmem_slot + 2);
   st.err = p.err;
   st.rank = P::PAIR ? cluster_ctarank() : 0u;
   st.unit_first = static_cast<int>(blockIdx.x) / P::NCTA;
@@ -348,8 +445,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(&st.tmem_empty[b], P::EPI_ARRIVALS);
     }
     mbar_init(st.drain, 1);
+    for (int s = 0; s < kSchedDepth; ++s) {
+      mbar_init(&st.sched_full[s], 1);
+      mbar_init(&st.sched_empty[s], P::SCHED_READERS);
+    }
     *st.abort = 0;
     fence_mbarrier_init();
+    if (blockIdx.x == 0) Cfg::on_launch(p);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);

@@ -29,6 +29,12 @@ constexpr int kGroupM = LLP_GROUP_M;
 #define LLP_PAIR_STAGES 6  // shared-memory pipeline stages in pair mode (32 KB each)
 #endif
 constexpr int kPairStages = LLP_PAIR_STAGES;
+#ifndef LLP_DYNAMIC_SCHED
+#define LLP_DYNAMIC_SCHED 3  // bit 0: grad_hidden, bit 1: grad_weight claim units in order from a ticket counter
+#endif
+#ifndef LLP_HALF_TILE
+#define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
+#endif
 
 // Resident work groups (CTA pairs, or CTAs in single mode) per GEMM kernel,
 // found once per device; the persistent grids never exceed them.
@@ -68,7 +74,13 @@ struct DzParams {
   unsigned int* err;
   long long vocab_start;  // global id of local vocab row 0 (vocab-parallel shards; 0 otherwise)
   long long global_V;     // global vocab size: decides which targets are valid
+  int* sched_reset;       // [kNumSchedCounters] ticket counters of the gradient GEMMs, zeroed at launch
 };
+
+// Ticket counters of the in-order scheduled gradient GEMMs (one per GEMM of a
+// backward), held in the backward workspace and zeroed by the dlogits kernel
+// that precedes them on the stream.
+constexpr int kNumSchedCounters = 2;
 
 struct GradGemmParams {
   int rows;          // M extent: N for grad_hidden, V for grad_weight
@@ -79,6 +91,7 @@ struct GradGemmParams {
   float* part;         // [nseg][rows][D] fp32 partials when nseg > 1 or f32_out
   unsigned int* err;
   int f32_out;         // 1: always write fp32 partials (a vocab shard's grad_hidden contribution)
+  int* sched;          // ticket counter, 0 at launch
 };
 
 // Launchers (return the launch error, never synchronise).  `units` is the

@@ -24,6 +24,7 @@ enum DeviceError : unsigned int {
   kDevTimeoutTmemEmpty = 4,  // MMA issuer waited too long for a drained accumulator
   kDevTimeoutDrain = 5,      // in-flight MMAs did not finish at teardown
   kDevTimeoutSelfTest = 6,   // the wait-timeout self-test gave up, as intended
+  kDevTimeoutSched = 7,      // a role waited too long for the next unit id (or for a free slot)
 };
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
@@ -70,6 +71,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// try_wait with cluster-scope acquire: orders this thread's later reads after
+// writes that a thread of the peer CTA made before its release-arrive.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Returns false (and raises
 // *abort) on timeout or when another role of this CTA has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -83,6 +98,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if ((it & 255u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > limit_ns) {
+        atomicCAS(err, 0u, code);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// mbar_wait with cluster-scope acquire (see mbar_try_wait_cluster).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  unsigned int* err, unsigned int code) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait_cluster(addr, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(addr, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
         atomicCAS(err, 0u, code);
         *abort = 1;
         return false;
@@ -284,6 +318,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Arrive on an mbarrier given by its shared::cluster address (own CTA or the peer).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 32-bit store into shared memory given by its shared::cluster address (own CTA or the peer).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on the
