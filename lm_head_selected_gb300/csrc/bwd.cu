@@ -178,7 +178,12 @@ struct DzCfg {
       }
       // rows >= N and columns >= V are clipped by the store's tensor map; a slab
       // that starts past the last row is not stored at all (warp-uniform)
-      if (row0 < p.N) epi_slab_store_2d(es, sbuf, v0 + 64 * q, row0);
+      if (row0 < p.N) {
+        if (LLP_DZ_STREAM)
+          epi_slab_store_2d_stream(es, sbuf, v0 + 64 * q, row0);
+        else
+          epi_slab_store_2d(es, sbuf, v0 + 64 * q, row0);
+      }
     }
   }
 

@@ -147,6 +147,19 @@ __device__ __forceinline__ void epi_slab_store_2d(EpiStore& es, uint32_t buf, in
   es.next ^= 1u;
 }
 
+// As epi_slab_store_2d, for an output that is streamed once through L2 (the
+// bf16 dlogits): stored with evict-first priority so it does not push out the
+// operand tiles that the running units still re-read.
+__device__ __forceinline__ void epi_slab_store_2d_stream(EpiStore& es, uint32_t buf, int x, int y) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (es.lane == 0) {
+    tma_store_2d_hint(es.map, buf, x, y, l2_policy_evict_first());
+    bulk_commit_group();
+  }
+  es.next ^= 1u;
+}
+
 __device__ __forceinline__ void epi_slab_store_3d(EpiStore& es, uint32_t buf, int x, int y, int z) {
   fence_proxy_async_smem();
   __syncwarp();

@@ -32,6 +32,9 @@ constexpr int kPairStages = LLP_PAIR_STAGES;
 #ifndef LLP_DYNAMIC_SCHED
 #define LLP_DYNAMIC_SCHED 3  // bit 0: grad_hidden, bit 1: grad_weight claim units in order from a ticket counter
 #endif
+#ifndef LLP_DZ_STREAM
+#define LLP_DZ_STREAM 1      // store the bf16 dlogits with L2 evict-first priority
+#endif
 #ifndef LLP_HALF_TILE
 #define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
 #endif

@@ -166,6 +166,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sm
                : "memory");
 }
 
+// Tensor store with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t smem_src, int x, int y,
+                                                  uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::
+                   "l"(reinterpret_cast<uint64_t>(map)),
+               "r"(smem_src), "r"(x), "r"(y), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t smem_src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
