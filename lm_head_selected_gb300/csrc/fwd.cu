@@ -158,26 +158,59 @@ struct FwdCfg {
   }
 };
 
+// One warp per row.  The lanes load the row's split partials and find the
+// maximum together (max is exact in any order); the terms exp(m_s - M) are
+// staged in shared memory and lane 0 folds them in ascending split order with
+// fused multiply-adds, so the row's sum is the same sequence of roundings
+// whatever N or the grid is.  A warp per row keeps a small batch (tens of
+// rows) from waiting on hundreds of dependent loads in one thread.
+constexpr int kMergeWarps = 8;    // rows per 256-thread block
+constexpr int kMergeChunk = 256;  // splits staged per pass
+
+__device__ __forceinline__ void merge_splits_warp(const FwdParams& p, int n, int lane, float* ps, float* ex, float& M,
+                                                  float& S) {
+  M = -INFINITY;
+  for (int s = lane; s < p.num_splits; s += 32) M = fmaxf(M, p.part_m[static_cast<size_t>(s) * p.N + n]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  S = 0.f;
+  for (int s0 = 0; s0 < p.num_splits; s0 += kMergeChunk) {
+    const int cnt = min(kMergeChunk, p.num_splits - s0);
+    for (int j = lane; j < cnt; j += 32) {
+      const size_t i = static_cast<size_t>(s0 + j) * p.N + n;
+      ps[j] = p.part_s[i];
+      ex[j] = exp2f((p.part_m[i] - M) * kLog2e);
+    }
+    __syncwarp();
+    if (lane == 0)
+      for (int j = 0; j < cnt; ++j) S = __fmaf_rn(ps[j], ex[j], S);
+    __syncwarp();
+  }
+  S = __shfl_sync(0xffffffffu, S, 0);
+}
+
 __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __restrict__ out_logp,
                                                         float* __restrict__ out_lse) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= p.N) return;
+  __shared__ float stage[kMergeWarps][2][kMergeChunk];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * kMergeWarps + warp;
+  if (n >= p.N) return;  // warp-uniform
   const long long t = p.targets[n];
   if (!target_valid(t, p.V, p.ignore_index)) {
-    out_logp[n] = 0.f;
-    out_lse[n] = -INFINITY;
+    if (lane == 0) {
+      out_logp[n] = 0.f;
+      out_lse[n] = -INFINITY;
+    }
     return;
   }
-  float M = -INFINITY;
-  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, p.part_m[static_cast<size_t>(s) * p.N + n]);
-  float S = 0.f;
-  for (int s = 0; s < p.num_splits; ++s) {
-    const size_t i = static_cast<size_t>(s) * p.N + n;
-    S += p.part_s[i] * exp2f((p.part_m[i] - M) * kLog2e);
+  float M, S;
+  merge_splits_warp(p, n, lane, stage[warp][0], stage[warp][1], M, S);
+  if (lane == 0) {
+    const float ls = logf(S);
+    out_lse[n] = M + ls;
+    out_logp[n] = (p.zt[n] - M) - ls;
   }
-  const float ls = logf(S);
-  out_lse[n] = M + ls;
-  out_logp[n] = (p.zt[n] - M) - ls;
 }
 
 // Vocab-parallel shard statistics ("Fused Linear LogP", Tensor Parallel Vocab
@@ -187,21 +220,21 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __re
 // else -inf.
 __global__ void __launch_bounds__(256) shard_stats_kernel(FwdParams p, float* __restrict__ out_max,
                                                           float* __restrict__ out_se, float* __restrict__ out_tl) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= p.N) return;
-  float M = -INFINITY;
-  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, p.part_m[static_cast<size_t>(s) * p.N + n]);
-  float S = 0.f;
-  for (int s = 0; s < p.num_splits; ++s) {
-    const size_t i = static_cast<size_t>(s) * p.N + n;
-    S += p.part_s[i] * exp2f((p.part_m[i] - M) * kLog2e);
+  __shared__ float stage[kMergeWarps][2][kMergeChunk];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * kMergeWarps + warp;
+  if (n >= p.N) return;  // warp-uniform
+  float M, S;
+  merge_splits_warp(p, n, lane, stage[warp][0], stage[warp][1], M, S);
+  if (lane == 0) {
+    const long long t = p.targets[n];
+    const long long tl = t - p.vocab_start;
+    const bool local = t != p.ignore_index && tl >= 0 && tl < static_cast<long long>(p.V);
+    out_max[n] = M;
+    out_se[n] = S;
+    out_tl[n] = local ? p.zt[n] : -INFINITY;
   }
-  const long long t = p.targets[n];
-  const long long tl = t - p.vocab_start;
-  const bool local = t != p.ignore_index && tl >= 0 && tl < static_cast<long long>(p.V);
-  out_max[n] = M;
-  out_se[n] = S;
-  out_tl[n] = local ? p.zt[n] : -INFINITY;
 }
 
 // Merge of R shards' (max, sum, target logit) in ascending rank order, then the
@@ -237,7 +270,7 @@ __global__ void __launch_bounds__(256) merge_shards_kernel(const float* __restri
 
 cudaError_t launch_shard_stats(const FwdParams& p, float* out_max, float* out_sumexp, float* out_tlogit,
                                cudaStream_t s) {
-  shard_stats_kernel<<<(p.N + 255) / 256, 256, 0, s>>>(p, out_max, out_sumexp, out_tlogit);
+  shard_stats_kernel<<<(p.N + kMergeWarps - 1) / kMergeWarps, 256, 0, s>>>(p, out_max, out_sumexp, out_tlogit);
   return cudaGetLastError();
 }
 
@@ -269,9 +302,7 @@ cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w
 }
 
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s) {
-  const int threads = 256;
-  const int blocks = (p.N + threads - 1) / threads;
-  fwd_merge_kernel<<<blocks, threads, 0, s>>>(p, out_logp, out_lse);
+  fwd_merge_kernel<<<(p.N + kMergeWarps - 1) / kMergeWarps, 256, 0, s>>>(p, out_logp, out_lse);
   return cudaGetLastError();
 }
 
