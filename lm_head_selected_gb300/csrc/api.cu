@@ -276,6 +276,13 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   return LLP_OK;
 }
 
+// K-blocks of a gradient GEMM's shortest unit (its last K segment).
+int64_t min_units_kblocks(const llp::GradGemmParams& p) {
+  const int64_t total = cdiv(p.K, llp::kTileK);
+  const int64_t rest = total - static_cast<int64_t>(p.nseg - 1) * p.kseg_blocks;
+  return rest < p.kseg_blocks ? rest : p.kseg_blocks;
+}
+
 // Backward launch sequence on validated arguments (N > 0, workspace sized by bwd_layout).
 // For a vocab shard: `weight` starts at global id vocab_start, targets are valid
 // against global_V, and grad_hidden_f32 (fp32 [N, D]) receives this shard's
@@ -342,7 +349,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
     p.err = dev->status_ptr;
     p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
-    p.sched = sched + 0;
+    p.sched = min_units_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
     if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
@@ -376,7 +383,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
     p.f32_out = 0;
     p.err = dev->status_ptr;
-    p.sched = sched + 1;
+    p.sched = min_units_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
     if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;

@@ -22,8 +22,10 @@
 // A unit of work is a run of `ntiles` consecutive output tiles that share A
 // rows (the forward's vocab split) or a single tile with a K range (a fixed K
 // segment of the gradient GEMMs).  CTAs (or pairs) take units either
-// round-robin (static) or, for configurations with DYNAMIC set, in ascending
-// order from a global ticket counter: the pair's producer draws the ticket and
+// round-robin (static) or, for configurations with DYNAMIC set and a launch
+// given a ticket counter, in ascending order from that counter (the host gives
+// one only when units are long enough to repay the hand-off, about a
+// microsecond per unit): the pair's producer draws the ticket and
 // hands the unit id to every other role through a small ring of slots in
 // shared memory.  In-order claiming keeps the units that share operands
 // running at the same time, so their operands are re-used from L2 instead of
@@ -229,13 +231,12 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
   int stage = 0;
   uint32_t phase = 0;
   const int num_units = Cfg::num_units(p);
+  const bool dyn = Cfg::DYNAMIC && Cfg::sched_counter(p) != nullptr;
   int ticket = 0;
-  if constexpr (Cfg::DYNAMIC) {
-    if (leader) ticket = atomicAdd(Cfg::sched_counter(p), 1);
-  }
+  if (dyn && leader) ticket = atomicAdd(Cfg::sched_counter(p), 1);
   for (int k = 0;; ++k) {
     int u;
-    if constexpr (Cfg::DYNAMIC)
+    if (dyn)
       u = leader ? publish_unit<Cfg>(st, k, ticket < num_units ? ticket : -1) : receive_unit<Cfg>(st, k, false);
     else
       u = static_unit<Cfg>(st, p, k);
@@ -248,12 +249,10 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
     for (int j = 0; j < ui.ntiles; ++j) {
       const int b_row = ui.n0 + j * Cfg::BN + static_cast<int>(st.rank) * b_rows;
       for (int kb = 0; kb < ui.nkb; ++kb) {
-        if constexpr (Cfg::DYNAMIC) {
-          // draw the next ticket a few k-blocks before the unit ends, so its
-          // latency hides behind the loads still to issue
-          if (leader && j == ui.ntiles - 1 && kb == (ui.nkb > 4 ? ui.nkb - 4 : 0))
-            ticket = atomicAdd(Cfg::sched_counter(p), 1);
-        }
+        // draw the next ticket a few k-blocks before the unit ends, so its
+        // latency hides behind the loads still to issue
+        if (dyn && leader && j == ui.ntiles - 1 && kb == (ui.nkb > 4 ? ui.nkb - 4 : 0))
+          ticket = atomicAdd(Cfg::sched_counter(p), 1);
         if (!mbar_wait(&st.empty[stage], phase ^ 1u, st.abort, st.err, kDevTimeoutEmpty)) return;
         const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
         const uint32_t sB = sA + P::A_BYTES;
@@ -316,9 +315,10 @@ __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cf
   int stage = 0;
   uint32_t phase = 0;
   uint32_t acc_i = 0;
+  const bool dyn = Cfg::DYNAMIC && Cfg::sched_counter(p) != nullptr;
   for (int k = 0;; ++k) {
     int u;
-    if constexpr (Cfg::DYNAMIC)
+    if (dyn)
       u = receive_unit<Cfg>(st, k, false);
     else
       u = static_unit<Cfg>(st, p, k);
@@ -383,9 +383,10 @@ __device__ __forceinline__ void run_epilogue(const SharedState& st, const CUtens
   es.lane = lane;
   uint32_t acc_i = 0;
   bool ok = true;
+  const bool dyn = Cfg::DYNAMIC && Cfg::sched_counter(p) != nullptr;
   for (int k = 0; ok; ++k) {
     int u;
-    if constexpr (Cfg::DYNAMIC)
+    if (dyn)
       u = receive_unit<Cfg>(st, k, true);
     else
       u = static_unit<Cfg>(st, p, k);
@@ -407,7 +408,7 @@ __device__ __forceinline__ void run_epilogue(const SharedState& st, const CUtens
       __syncwarp();
       if (lane == 0) {
         if (P::PAIR)
-          mbar_arrive_cluster(map_to_cta(smem_u32(&st.tmem_empty[buf]), 0));
+          LLP_TMEM_RELEASE(map_to_cta(smem_u32(&st.tmem_empty[buf]), 0));
         else
           mbar_arrive(&st.tmem_empty[buf]);
       }

@@ -35,6 +35,13 @@ constexpr int kPairStages = LLP_PAIR_STAGES;
 #ifndef LLP_DZ_STREAM
 #define LLP_DZ_STREAM 1      // store the bf16 dlogits with L2 evict-first priority
 #endif
+#ifndef LLP_TMEM_RELEASE
+#define LLP_TMEM_RELEASE mbar_arrive_remote
+#endif
+#ifndef LLP_DYN_MIN_KB
+#define LLP_DYN_MIN_KB 128   // in-order claiming only for units of at least this many k-blocks
+#endif
+constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 #ifndef LLP_HALF_TILE
 #define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
 #endif
@@ -94,7 +101,7 @@ struct GradGemmParams {
   float* part;         // [nseg][rows][D] fp32 partials when nseg > 1 or f32_out
   unsigned int* err;
   int f32_out;         // 1: always write fp32 partials (a vocab shard's grad_hidden contribution)
-  int* sched;          // ticket counter, 0 at launch
+  int* sched;          // ticket counter, 0 at launch; nullptr: round-robin units
 };
 
 // Launchers (return the launch error, never synchronise).  `units` is the

@@ -334,6 +334,13 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// Arrive on an mbarrier given by its shared::cluster address with the default
+// (release, CTA-scope) semantics: enough where the arrive only hands over
+// tensor-memory or tensor-core state that tcgen05 fences already order.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on the
 // mbarrier at `bar_cluster_addr`, which may live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
