@@ -148,6 +148,25 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fp16 inputs ("Fused Linear LogP", Tensor Contract: hidden and lm_head_weight
+ * may be bf16 or fp16).  Same arguments, workspaces, checks and results as
+ * linear_logp_fwd / linear_logp_bwd, except that hidden and weight are IEEE
+ * fp16 [N, D] / [V, D] and grad_hidden / grad_weight are written in fp16.  The
+ * dlogits workspace then holds fp16 too, since both operands of a tensor-core
+ * product have one type; every accumulation stays fp32.  fp16 cannot hold a
+ * dlogit above 65504 in magnitude: |grad_logp / temperature| must stay below
+ * that.  fp32 inputs are not accepted by any entry point (the Python wrapper
+ * refuses them).
+ */
+int linear_logp_fwd_f16(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                        const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                        float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream);
+int linear_logp_bwd_f16(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                        const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                        int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Row-subset (indexed) variants ("recursive deterministic LogP autograd on
  * B200", What: indexed semantics; "add backward support for fused logp CUDA
  * kernels", Implementation details: zero gradients for rows omitted by indexed

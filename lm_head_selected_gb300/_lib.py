@@ -40,6 +40,8 @@ EXPORTED = (
     "linear_logp_merge_shards",
     "linear_logp_bwd_shard",
     "linear_logp_sum_partials",
+    "linear_logp_fwd_f16",
+    "linear_logp_bwd_f16",
 )
 # include/fused_logp.h (logits-input op, same library)
 EXPORTED_FUSED = (
@@ -91,6 +93,10 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_bwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _p, _p, _p,
                                         _size, _p]
         lib.linear_logp_bwd.restype = ctypes.c_int
+        lib.linear_logp_fwd_f16.argtypes = lib.linear_logp_fwd.argtypes
+        lib.linear_logp_fwd_f16.restype = ctypes.c_int
+        lib.linear_logp_bwd_f16.argtypes = lib.linear_logp_bwd.argtypes
+        lib.linear_logp_bwd_f16.restype = ctypes.c_int
         lib.linear_logp_status_string.argtypes = [ctypes.c_int]
         lib.linear_logp_status_string.restype = ctypes.c_char_p
         lib.linear_logp_device_status.argtypes = [_p, ctypes.POINTER(ctypes.c_uint)]

@@ -159,13 +159,15 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, b
   return L;
 }
 
+// 2-D map of a 16-bit matrix: bf16, or IEEE fp16 when f16.
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-             uint32_t box_inner, uint32_t box_outer) {
+             uint32_t box_inner, uint32_t box_outer, bool f16 = false) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                              const_cast<void*>(base), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
@@ -186,7 +188,8 @@ int make_map_part(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
 
 // Output map of a gradient [rows][D] (bf16) or of its segment partials.
 int make_map_grad_out(CUtensorMap* m, const llp::GradGemmParams& p) {
-  if (p.nseg == 1 && !p.f32_out) return make_map(m, p.out, p.D, p.rows, static_cast<uint64_t>(p.D) * 2, 64, 32);
+  if (p.nseg == 1 && !p.f32_out)
+    return make_map(m, p.out, p.D, p.rows, static_cast<uint64_t>(p.D) * 2, 64, 32, p.f16 != 0);
   return make_map_part(m, p.part, p.D, p.rows, p.nseg);
 }
 
@@ -240,11 +243,11 @@ void rec_mark(cudaStream_t s, int id) {
 int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const float* bias, const int64_t* targets,
              const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index, float* out_logp,
              float* out_lse, uint8_t* ws, cudaStream_t s, int64_t vocab_start = 0, float* sh_max = nullptr,
-             float* sh_se = nullptr, float* sh_tl = nullptr) {
+             float* sh_se = nullptr, float* sh_tl = nullptr, bool f16 = false) {
   const FwdLayout L = fwd_layout(N, V);
   CUtensorMap tm_h, tm_w;
-  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return LLP_ERR_CUDA;
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
@@ -263,6 +266,7 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.err = dev->status_ptr;
   p.vocab_start = vocab_start;
   p.global_V = V;
+  p.f16 = f16 ? 1 : 0;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   rec_mark(s, -1);
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
@@ -290,7 +294,8 @@ int64_t min_units_kblocks(const llp::GradGemmParams& p) {
 int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
              const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V,
              int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias, uint8_t* ws,
-             cudaStream_t s, int64_t vocab_start = 0, int64_t global_V = -1, float* grad_hidden_f32 = nullptr) {
+             cudaStream_t s, int64_t vocab_start = 0, int64_t global_V = -1, float* grad_hidden_f32 = nullptr,
+             bool f16 = false) {
   if (global_V < 0) global_V = V;
   const bool want_gb = grad_bias != nullptr;
   const bool want_gh = grad_hidden != nullptr || grad_hidden_f32 != nullptr;
@@ -302,8 +307,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   // B1: dlogits (+ grad_bias partials)
   {
     CUtensorMap tm_h, tm_w;
-    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return LLP_ERR_CUDA;
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -324,10 +329,11 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.vocab_start = vocab_start;
     p.global_V = global_V;
     p.sched_reset = sched;
+    p.f16 = f16 ? 1 : 0;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
     CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
-    if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32, f16) != LLP_OK) return LLP_ERR_CUDA;
     if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
     rec_mark(s, kKDlogits);
   }
@@ -335,8 +341,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   // B2: grad_hidden = dz . W over fixed vocab segments
   if (want_gh) {
     CUtensorMap tm_dz, tm_w_mn;
-    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) return LLP_ERR_CUDA;
     llp::GradGemmParams p;
     p.rows = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -349,6 +355,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
     p.err = dev->status_ptr;
     p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
+    p.f16 = f16 ? 1 : 0;
     p.sched = min_units_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
     if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
@@ -360,7 +367,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     if (p.nseg > 1) {
       const cudaError_t e =
           p.f32_out ? llp::launch_segment_sum_f32(p.part, p.nseg, static_cast<long long>(N) * D, grad_hidden_f32, s)
-                    : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s);
+                    : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s, p.f16);
       if (e != cudaSuccess) return LLP_ERR_CUDA;
       rec_mark(s, kKSegSumHidden);
     }
@@ -369,8 +376,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   // B3: grad_weight = dz^T . h over fixed token segments
   if (grad_weight != nullptr) {
     CUtensorMap tm_dz_mn, tm_h_mn;
-    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) return LLP_ERR_CUDA;
     llp::GradGemmParams p;
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
@@ -382,6 +389,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.out = static_cast<__nv_bfloat16*>(grad_weight);
     p.part = L.has_dw ? reinterpret_cast<float*>(ws + L.dw_part) : nullptr;
     p.f32_out = 0;
+    p.f16 = f16 ? 1 : 0;
     p.err = dev->status_ptr;
     p.sched = min_units_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
@@ -391,7 +399,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       return LLP_ERR_CUDA;
     rec_mark(s, kKGradWeight);
     if (p.nseg > 1) {
-      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s) != cudaSuccess)
+      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s, p.f16) != cudaSuccess)
         return LLP_ERR_CUDA;
       rec_mark(s, kKSegSumWeight);
     }
@@ -439,9 +447,10 @@ const char* linear_logp_status_string(int status) {
   }
 }
 
-int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
-                    const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
-                    float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream) {
+// hidden / weight are bf16, or IEEE fp16 when f16.
+static int fwd_entry(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                     const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                     float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream, bool f16) {
   int st = check_shapes(N, D, V);
   if (st != LLP_OK) return st;
   if (N == 0) return LLP_OK;  // nothing to compute; per-token pointers may be NULL
@@ -458,13 +467,29 @@ int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, c
   if ((st = init_device(&dev)) != LLP_OK) return st;
   if ((st = load_encode_fn()) != LLP_OK) return st;
   return fwd_core(dev, hidden, weight, bias, targets, temperature, N, D, V, ignore_index, out_logp, out_lse,
-                  static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+                  static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream), 0, nullptr, nullptr, nullptr,
+                  f16);
 }
 
-int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
-                    const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
-                    int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                    const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                    float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_entry(hidden, weight, bias, targets, temperature, N, D, V, ignore_index, out_logp, out_lse, workspace,
+                   workspace_bytes, stream, false);
+}
+
+int linear_logp_fwd_f16(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                        const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                        float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_entry(hidden, weight, bias, targets, temperature, N, D, V, ignore_index, out_logp, out_lse, workspace,
+                   workspace_bytes, stream, true);
+}
+
+// hidden / weight / grad_hidden / grad_weight are bf16, or IEEE fp16 when f16.
+static int bwd_entry(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                     const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                     int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
+                     void* workspace, size_t workspace_bytes, void* stream, bool f16) {
   int st = check_shapes(N, D, V);
   if (st != LLP_OK) return st;
   if (grad_bias != nullptr && bias == nullptr) return LLP_ERR_NULL_POINTER;
@@ -497,7 +522,23 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
   if ((st = init_device(&dev)) != LLP_OK) return st;
   if ((st = load_encode_fn()) != LLP_OK) return st;
   return bwd_core(dev, grad_logp, saved_lse, hidden, weight, bias, targets, temperature, N, D, V, ignore_index,
-                  grad_hidden, grad_weight, grad_bias, static_cast<uint8_t*>(workspace), s);
+                  grad_hidden, grad_weight, grad_bias, static_cast<uint8_t*>(workspace), s, 0, -1, nullptr, f16);
+}
+
+int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                    const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                    int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_entry(grad_logp, saved_lse, hidden, weight, bias, targets, temperature, N, D, V, ignore_index,
+                   grad_hidden, grad_weight, grad_bias, workspace, workspace_bytes, stream, false);
+}
+
+int linear_logp_bwd_f16(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                        const float* bias, const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                        int64_t V, int64_t ignore_index, void* grad_hidden, void* grad_weight, float* grad_bias,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_entry(grad_logp, saved_lse, hidden, weight, bias, targets, temperature, N, D, V, ignore_index,
+                   grad_hidden, grad_weight, grad_bias, workspace, workspace_bytes, stream, true);
 }
 
 // ----------------------------------------------------------------------------
@@ -909,6 +950,7 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   p.err = dev->status_ptr;
   p.vocab_start = 0;
   p.global_V = V;
+  p.f16 = 0;
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;

@@ -53,6 +53,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two floats rounded to the path's 16-bit type (fp16 when f16, else bf16).
+__device__ __forceinline__ uint32_t pack16x2(bool f16, float a, float b) {
+  return f16 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+}
+
 // ----------------------------------------------------------------------------
 // B1: dlogits
 // ----------------------------------------------------------------------------
@@ -130,6 +140,7 @@ struct DzCfg {
     const bool full = (v0 + BN) <= p.V;
     const bool bias_vec = full && (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     const int blk = (ui.m0 + row) >> 5;  // 32-row block of this warp
+    const bool f16 = p.f16 != 0;
     const int row0 = ui.m0 + row - lane;  // first token row of this warp's slab
 #pragma unroll 1
     for (int q = 0; q < BN / 64; ++q) {  // 64-column slabs of dz, one TMA store each
@@ -167,9 +178,9 @@ struct DzCfg {
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          epi_slab_put(sbuf, lane, 4 * h + k, pack_bf16x2(z[8 * k + 0], z[8 * k + 1]),
-                       pack_bf16x2(z[8 * k + 2], z[8 * k + 3]), pack_bf16x2(z[8 * k + 4], z[8 * k + 5]),
-                       pack_bf16x2(z[8 * k + 6], z[8 * k + 7]));
+          epi_slab_put(sbuf, lane, 4 * h + k, pack16x2(f16, z[8 * k + 0], z[8 * k + 1]),
+                       pack16x2(f16, z[8 * k + 2], z[8 * k + 3]), pack16x2(f16, z[8 * k + 4], z[8 * k + 5]),
+                       pack16x2(f16, z[8 * k + 6], z[8 * k + 7]));
         if (HAS_BIAS && p.gb_part != nullptr) {  // warp-uniform
           const float colsum = warp_column_sums(z, lane);
           const int v = vc + lane;
@@ -251,6 +262,7 @@ struct GradCfg {
     const int row0 = ui.m0 + row - lane;
     if (row0 >= p.rows) return;  // this warp's rows are all past the end (warp-uniform)
     if (p.nseg == 1 && !p.f32_out) {
+      const bool f16 = p.f16 != 0;
 #pragma unroll 1
       for (int q = 0; q < BN / 64; ++q) {
         const int d0 = ui.n0 + 64 * q;
@@ -262,9 +274,9 @@ struct GradCfg {
           tmem_load_32cols(taddr + 64 * q + 32 * h, a);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            epi_slab_put(sbuf, lane, 4 * h + k, pack_bf16x2(a[8 * k + 0], a[8 * k + 1]),
-                         pack_bf16x2(a[8 * k + 2], a[8 * k + 3]), pack_bf16x2(a[8 * k + 4], a[8 * k + 5]),
-                         pack_bf16x2(a[8 * k + 6], a[8 * k + 7]));
+            epi_slab_put(sbuf, lane, 4 * h + k, pack16x2(f16, a[8 * k + 0], a[8 * k + 1]),
+                         pack16x2(f16, a[8 * k + 2], a[8 * k + 3]), pack16x2(f16, a[8 * k + 4], a[8 * k + 5]),
+                         pack16x2(f16, a[8 * k + 6], a[8 * k + 7]));
         }
         epi_slab_store_2d(es, sbuf, d0, row0);
       }
@@ -288,9 +300,9 @@ struct GradCfg {
   static __device__ __forceinline__ void unit_end(const Params&, const UnitInfo&, int, int, RowState&) {}
 };
 
-// out[i] = bf16( sum_{s ascending} part[s][i] ), 4 elements per thread step.
+// out[i] = bf16 (fp16 when f16) of sum_{s ascending} part[s][i], 4 elements per thread step.
 __global__ void __launch_bounds__(256) segment_sum_kernel(const float* __restrict__ part, int nseg, long long count,
-                                                          __nv_bfloat16* __restrict__ out) {
+                                                          __nv_bfloat16* __restrict__ out, int f16) {
   const long long n4 = count / 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     float4 acc = reinterpret_cast<const float4*>(part)[i];
@@ -302,8 +314,8 @@ __global__ void __launch_bounds__(256) segment_sum_kernel(const float* __restric
       acc.w += v.w;
     }
     uint2 w;
-    w.x = pack_bf16x2(acc.x, acc.y);
-    w.y = pack_bf16x2(acc.z, acc.w);
+    w.x = pack16x2(f16 != 0, acc.x, acc.y);
+    w.y = pack16x2(f16 != 0, acc.z, acc.w);
     reinterpret_cast<uint2*>(out)[i] = w;
   }
 }
@@ -366,12 +378,13 @@ cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& t
   return launch_units<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, tm_out, p, units, caps.gw_groups, s);
 }
 
-cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s) {
+cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s,
+                               int f16) {
   const int threads = 256;
   long long blocks = (count / 4 + threads - 1) / threads;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
-  segment_sum_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
+  segment_sum_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out, f16);
   return cudaGetLastError();
 }
 

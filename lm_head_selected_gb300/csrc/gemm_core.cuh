@@ -310,8 +310,9 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 template <class Cfg>
 __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
   using P = Plan<Cfg>;
-  constexpr uint32_t idesc_full = make_idesc_bf16_f32(P::UM, Cfg::BN, Cfg::A_MN, Cfg::B_MN);
-  constexpr uint32_t idesc_half = make_idesc_bf16_f32(P::UM, Cfg::BN / 2, Cfg::A_MN, Cfg::B_MN);
+  // both operands have the same 16-bit type (the params' f16 flag)
+  const uint32_t idesc_full = make_idesc_16_f32(P::UM, Cfg::BN, Cfg::A_MN, Cfg::B_MN, p.f16 != 0);
+  const uint32_t idesc_half = make_idesc_16_f32(P::UM, Cfg::BN / 2, Cfg::A_MN, Cfg::B_MN, p.f16 != 0);
   int stage = 0;
   uint32_t phase = 0;
   uint32_t acc_i = 0;

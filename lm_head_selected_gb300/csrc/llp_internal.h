@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -68,6 +69,7 @@ struct FwdParams {
   unsigned int* err;
   long long vocab_start;  // global id of local vocab row 0 (vocab-parallel shards; 0 otherwise)
   long long global_V;     // global vocab size (== V unless sharded)
+  int f16;                // hidden / weight are IEEE fp16 (else bf16)
 };
 
 struct DzParams {
@@ -79,12 +81,13 @@ struct DzParams {
   long long ignore_index;
   const float* grad_logp;
   const float* lse;
-  __nv_bfloat16* dz;  // [N][V_pad]
+  __nv_bfloat16* dz;  // [N][V_pad], bf16 (or fp16 when f16; the two operands of a GEMM share one type)
   float* gb_part;     // [num_m*4][V]: per 32-row block column sums of dz (bias only)
   unsigned int* err;
   long long vocab_start;  // global id of local vocab row 0 (vocab-parallel shards; 0 otherwise)
   long long global_V;     // global vocab size: decides which targets are valid
   int* sched_reset;       // [kNumSchedCounters] ticket counters of the gradient GEMMs, zeroed at launch
+  int f16;                // hidden / weight / dz are IEEE fp16 (else bf16)
 };
 
 // Ticket counters of the in-order scheduled gradient GEMMs (one per GEMM of a
@@ -97,11 +100,12 @@ struct GradGemmParams {
   int D;             // output columns
   int K;             // reduction extent: V for grad_hidden, N for grad_weight
   int num_m, num_d, nseg, kseg_blocks;
-  __nv_bfloat16* out;  // [rows][D] bf16 when nseg == 1 and !f32_out
+  __nv_bfloat16* out;  // [rows][D] bf16 (fp16 when f16) when nseg == 1 and !f32_out
   float* part;         // [nseg][rows][D] fp32 partials when nseg > 1 or f32_out
   unsigned int* err;
   int f32_out;         // 1: always write fp32 partials (a vocab shard's grad_hidden contribution)
   int* sched;          // ticket counter, 0 at launch; nullptr: round-robin units
+  int f16;             // operands and the 16-bit output are IEEE fp16 (else bf16)
 };
 
 // Launchers (return the launch error, never synchronise).  `units` is the
@@ -165,7 +169,9 @@ cudaError_t scatter_selected_outputs(const RowSelection& sel, const float* c_log
 cudaError_t scatter_selected_grad_hidden(const RowSelection& sel, int N, int D, const __nv_bfloat16* c_gh,
                                          __nv_bfloat16* gh, cudaStream_t s);
 
-cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s);
+// out: bf16, or fp16 when f16 != 0
+cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s,
+                               int f16 = 0);
 cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s);
 
 }  // namespace llp

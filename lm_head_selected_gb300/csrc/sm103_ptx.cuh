@@ -291,12 +291,12 @@ __device__ __forceinline__ uint64_t make_smem_desc_sw128(uint32_t saddr, uint32_
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
-// a_mn / b_mn select MN-major (transposed) operands.
-__host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor for kind::f16 with 16-bit A/B (bf16, or IEEE fp16
+// when f16) and an fp32 accumulator.  a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t make_idesc_16_f32(int M, int N, bool a_mn, bool b_mn, bool f16) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)                    // A format: f16 = 0, bf16 = 1
+         | ((f16 ? 0u : 1u) << 10)                   // B format: same as A
          | ((a_mn ? 1u : 0u) << 15)                  // A major
          | ((b_mn ? 1u : 0u) << 16)                  // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8

@@ -2,12 +2,14 @@
 
 PyTorch supplies device memory and the current stream; every step of the
 computation runs in the CUDA kernels of ``liblinear_logp.so``.  Inputs are
-checked here and rejected (no fallback, no casting): hidden/weight bf16,
+checked here and rejected (no fallback, no casting): hidden/weight bf16 (or
+both fp16 for the plain forward / backward and ``linear_logp``),
 bias/temperature/grad fp32, targets int64, all contiguous on one CUDA device.
 
 Entry points mirror the C ABI names:
   * ``linear_logp_fwd``  -> (logp [N] fp32, lse [N] fp32)
-  * ``linear_logp_bwd``  -> (grad_hidden bf16 | None, grad_weight bf16 | None, grad_bias fp32 | None)
+  * ``linear_logp_bwd``  -> (grad_hidden | None, grad_weight | None, grad_bias fp32 | None), the
+    16-bit gradients in the inputs' dtype
   * ``linear_logp``      -> autograd-aware op with leading shapes, the interface
     of "Fused Linear LogP" (Entry Point): hidden [B,S,D] or [N,D], targets [B,S]
     or [N], optional bias; gradients flow into hidden, weight and bias.
@@ -45,12 +47,13 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device, 
         raise ValueError(f"{name} must be contiguous")
 
 
-def _check_inputs(hidden, weight, targets, bias, temperature):
+def _check_inputs(hidden, weight, targets, bias, temperature, allow_f16=False):
     if not isinstance(hidden, torch.Tensor) or hidden.device.type != "cuda":
         raise ValueError("hidden must be a CUDA tensor; this op has no CPU path")
     dev = hidden.device
-    _need(hidden, "hidden", torch.bfloat16, dev, 2)
-    _need(weight, "weight", torch.bfloat16, dev, 2)
+    dt = torch.float16 if (allow_f16 and hidden.dtype == torch.float16) else torch.bfloat16
+    _need(hidden, "hidden", dt, dev, 2)
+    _need(weight, "weight", dt, dev, 2)
     N, D = hidden.shape
     V = weight.shape[0]
     if weight.shape[1] != D:
@@ -89,8 +92,9 @@ def linear_logp_fwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.T
                     bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
                     ignore_index: int = IGNORE_INDEX, workspace: Optional[torch.Tensor] = None,
                     out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
-    """Per-token log-prob of the target and the row log-sum-exp (both fp32 [N])."""
-    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    """Per-token log-prob of the target and the row log-sum-exp (both fp32 [N]).
+    hidden / weight are both bf16 or both fp16."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature, allow_f16=True)
     lib = _lib.load()
     if out is None:
         logp = torch.empty(N, dtype=torch.float32, device=dev)
@@ -99,10 +103,10 @@ def linear_logp_fwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.T
         logp, lse = out
     nbytes = int(lib.linear_logp_fwd_workspace_bytes(N, D, V))
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.linear_logp_fwd(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), _ptr(temperature),
-                             N, D, V, int(ignore_index), _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(),
-                             _stream(dev))
-    _lib.check("linear_logp_fwd", st)
+    name = "linear_logp_fwd_f16" if hidden.dtype == torch.float16 else "linear_logp_fwd"
+    st = getattr(lib, name)(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), _ptr(temperature),
+                            N, D, V, int(ignore_index), _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev))
+    _lib.check(name, st)
     return logp, lse
 
 
@@ -132,22 +136,24 @@ def linear_logp_bwd(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hidden: to
                     temperature: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,
                     need_hidden: bool = True, need_weight: bool = True, need_bias: bool = True,
                     workspace: Optional[torch.Tensor] = None):
-    """Gradients of sum_n grad_logp[n] * logp[n] w.r.t. hidden, weight and bias."""
-    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    """Gradients of sum_n grad_logp[n] * logp[n] w.r.t. hidden, weight and bias
+    (hidden / weight gradients in the inputs' dtype, bf16 or fp16)."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature, allow_f16=True)
     _need(grad_logp, "grad_logp", torch.float32, dev, 1)
     _need(saved_lse, "saved_lse", torch.float32, dev, 1)
     if grad_logp.shape[0] != N or saved_lse.shape[0] != N:
         raise ValueError("grad_logp and saved_lse must have N entries")
     lib = _lib.load()
-    gh = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if need_hidden else None
-    gw = torch.empty((V, D), dtype=torch.bfloat16, device=dev) if need_weight else None
+    gh = torch.empty((N, D), dtype=hidden.dtype, device=dev) if need_hidden else None
+    gw = torch.empty((V, D), dtype=hidden.dtype, device=dev) if need_weight else None
     gb = torch.empty(V, dtype=torch.float32, device=dev) if (need_bias and bias is not None) else None
     nbytes = int(lib.linear_logp_bwd_workspace_bytes(N, D, V, int(bias is not None)))
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.linear_logp_bwd(_ptr(grad_logp), _ptr(saved_lse), _ptr(hidden), _ptr(weight), _ptr(bias),
-                             _ptr(targets), _ptr(temperature), N, D, V, int(ignore_index),
-                             _ptr(gh), _ptr(gw), _ptr(gb), _ptr(ws), ws.numel(), _stream(dev))
-    _lib.check("linear_logp_bwd", st)
+    name = "linear_logp_bwd_f16" if hidden.dtype == torch.float16 else "linear_logp_bwd"
+    st = getattr(lib, name)(_ptr(grad_logp), _ptr(saved_lse), _ptr(hidden), _ptr(weight), _ptr(bias),
+                            _ptr(targets), _ptr(temperature), N, D, V, int(ignore_index),
+                            _ptr(gh), _ptr(gw), _ptr(gb), _ptr(ws), ws.numel(), _stream(dev))
+    _lib.check(name, st)
     return gh, gw, gb
 
 
@@ -237,9 +243,10 @@ def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tenso
                 ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
     """log_softmax((hidden @ weight^T + bias) / temperature)[targets], fp32, with autograd.
 
-    hidden [..., D] bf16, weight [V, D] bf16, targets [...] int64, bias [V] fp32,
-    temperature [...] fp32 (per token).  Returns fp32 with the leading shape of
-    targets.  Gradients reach hidden and weight as bf16 and bias as fp32.
+    hidden [..., D] and weight [V, D] both bf16 or both fp16, targets [...] int64,
+    bias [V] fp32, temperature [...] fp32 (per token).  Returns fp32 with the
+    leading shape of targets.  Gradients reach hidden and weight in their dtype
+    and bias as fp32.
     """
     lead = targets.shape
     D = hidden.shape[-1]

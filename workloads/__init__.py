@@ -85,10 +85,12 @@ def make_inputs(
     n_ignore: int = 0,
     n_out_of_range: int = 0,
     grad_std: Optional[float] = None,
+    dtype: torch.dtype = torch.bfloat16,
 ) -> Inputs:
     """Generic seeded problem.
 
-    hidden ~ N(0, hidden_std^2) and weight ~ N(0, weight_std^2), rounded to bf16;
+    hidden ~ N(0, hidden_std^2) and weight ~ N(0, weight_std^2), rounded to
+    ``dtype`` (bf16, or fp16);
     bias ~ N(0, bias_std^2) fp32 when ``bias_std`` is given; per-row temperature
     ~ U[lo, hi] when ``temperature_range`` is given; targets uniform in [0, V) with
     ``n_ignore`` rows set to the ignore index and ``n_out_of_range`` rows set to
@@ -96,8 +98,8 @@ def make_inputs(
     ``grad_std`` is given, then N(0, grad_std^2).
     """
     g = _gen(seed)
-    hidden = _normal((N, D), hidden_std, g).to(torch.bfloat16)
-    weight = _normal((V, D), weight_std, g).to(torch.bfloat16)
+    hidden = _normal((N, D), hidden_std, g).to(dtype)
+    weight = _normal((V, D), weight_std, g).to(dtype)
     bias = None if bias_std is None else _normal((V,), bias_std, g)
     targets = torch.randint(0, V, (N,), generator=g, dtype=torch.int64)
     if N and (n_ignore or n_out_of_range):
