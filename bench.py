@@ -59,9 +59,9 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by hash).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "6de36ad7301459c2",
-    "bytes_per_launch": {"fwd_partials": 2325871872 + 36875520, "dlogits": 6795861504 + 4265242624,
-                         "grad_hidden": 24571427328 + 694773760, "grad_weight": 17684590592 + 695674112},
+    "sources_sha": "4b631b28381aa4d9",
+    "bytes_per_launch": {"fwd_partials": 1837079296 + 37159424, "dlogits": 5396595712 + 4273137920,
+                         "grad_hidden": 23727052544 + 698042880, "grad_weight": 14363210240 + 700922112},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")

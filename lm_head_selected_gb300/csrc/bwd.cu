@@ -170,7 +170,7 @@ struct DzCfg {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float zz = z[i] * rs.inv_tau;
-          const float pr = exp2f((zz - rs.lse) * kLog2eB);
+          const float pr = epi_exp2((zz - rs.lse) * kLog2eB);
           const float oh = (vc + i == rs.t) ? 1.f : 0.f;
           float d = rs.gs * (oh - pr);
           if (!rs.valid || (!full && vc + i >= p.V)) d = 0.f;

@@ -138,12 +138,12 @@ struct FwdCfg {
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        a0 += exp2f((z[i + 0] - mn) * kLog2e);
-        a1 += exp2f((z[i + 1] - mn) * kLog2e);
-        a2 += exp2f((z[i + 2] - mn) * kLog2e);
-        a3 += exp2f((z[i + 3] - mn) * kLog2e);
+        a0 += epi_exp2((z[i + 0] - mn) * kLog2e);
+        a1 += epi_exp2((z[i + 1] - mn) * kLog2e);
+        a2 += epi_exp2((z[i + 2] - mn) * kLog2e);
+        a3 += epi_exp2((z[i + 3] - mn) * kLog2e);
       }
-      rs.s = rs.s * exp2f((rs.m - mn) * kLog2e) + ((a0 + a1) + (a2 + a3));
+      rs.s = rs.s * epi_exp2((rs.m - mn) * kLog2e) + ((a0 + a1) + (a2 + a3));
       rs.m = mn;
     }
   }
@@ -158,59 +158,68 @@ struct FwdCfg {
   }
 };
 
-// One warp per row.  The lanes load the row's split partials and find the
-// maximum together (max is exact in any order); the terms exp(m_s - M) are
-// staged in shared memory and lane 0 folds them in ascending split order with
-// fused multiply-adds, so the row's sum is the same sequence of roundings
-// whatever N or the grid is.  A warp per row keeps a small batch (tens of
-// rows) from waiting on hundreds of dependent loads in one thread.
-constexpr int kMergeWarps = 8;    // rows per 256-thread block
-constexpr int kMergeChunk = 256;  // splits staged per pass
+// A block merges 32 rows: lane l of every warp serves row n0 + l, and the 8
+// warps split the vocab-split range, so every partial load is a coalesced
+// 128-byte row segment.  The maximum is combined across warps (exact in any
+// order); the terms exp(m_s - M) are staged in shared memory and lane l of warp
+// 0 folds them in ascending split order with fused multiply-adds, so a row's
+// sum is the same sequence of roundings whatever N or the grid is.
+constexpr int kMergeRows = 32;   // rows per 256-thread block
+constexpr int kMergeWarps = 8;   // warps sharing a row's splits
+constexpr int kMergeChunk = 64;  // splits staged per pass
 
-__device__ __forceinline__ void merge_splits_warp(const FwdParams& p, int n, int lane, float* ps, float* ex, float& M,
-                                                  float& S) {
-  M = -INFINITY;
-  for (int s = lane; s < p.num_splits; s += 32) M = fmaxf(M, p.part_m[static_cast<size_t>(s) * p.N + n]);
+struct MergeSmem {
+  float red[kMergeWarps][kMergeRows];
+  float ps[kMergeChunk][kMergeRows];
+  float ex[kMergeChunk][kMergeRows];
+};
+
+// Returns (M, S) of row n in lanes of warp 0 (other warps: undefined).  All
+// threads of the block must call it.
+__device__ __forceinline__ void merge_splits_block(const FwdParams& p, int n, MergeSmem& sm, float& M, float& S) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const bool valid = n < p.N;
+  float mx = -INFINITY;
+  if (valid)
+    for (int s = w; s < p.num_splits; s += kMergeWarps) mx = fmaxf(mx, p.part_m[static_cast<size_t>(s) * p.N + n]);
+  sm.red[w][lane] = mx;
+  __syncthreads();
+  M = sm.red[0][lane];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  for (int k = 1; k < kMergeWarps; ++k) M = fmaxf(M, sm.red[k][lane]);
   S = 0.f;
   for (int s0 = 0; s0 < p.num_splits; s0 += kMergeChunk) {
     const int cnt = min(kMergeChunk, p.num_splits - s0);
-    for (int j = lane; j < cnt; j += 32) {
-      const size_t i = static_cast<size_t>(s0 + j) * p.N + n;
-      ps[j] = p.part_s[i];
-      ex[j] = exp2f((p.part_m[i] - M) * kLog2e);
-    }
-    __syncwarp();
-    if (lane == 0)
-      for (int j = 0; j < cnt; ++j) S = __fmaf_rn(ps[j], ex[j], S);
-    __syncwarp();
+    if (valid)
+      for (int j = w; j < cnt; j += kMergeWarps) {
+        const size_t i = static_cast<size_t>(s0 + j) * p.N + n;
+        sm.ps[j][lane] = p.part_s[i];
+        sm.ex[j][lane] = exp2f((p.part_m[i] - M) * kLog2e);
+      }
+    __syncthreads();
+    if (w == 0 && valid)
+      for (int j = 0; j < cnt; ++j) S = __fmaf_rn(sm.ps[j][lane], sm.ex[j][lane], S);
+    __syncthreads();
   }
-  S = __shfl_sync(0xffffffffu, S, 0);
 }
 
 __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __restrict__ out_logp,
                                                         float* __restrict__ out_lse) {
-  __shared__ float stage[kMergeWarps][2][kMergeChunk];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * kMergeWarps + warp;
-  if (n >= p.N) return;  // warp-uniform
+  __shared__ MergeSmem sm;
+  const int n = blockIdx.x * kMergeRows + (threadIdx.x & 31);
+  float M, S;
+  merge_splits_block(p, n, sm, M, S);
+  if (threadIdx.x >= 32 || n >= p.N) return;
   const long long t = p.targets[n];
   if (!target_valid(t, p.V, p.ignore_index)) {
-    if (lane == 0) {
-      out_logp[n] = 0.f;
-      out_lse[n] = -INFINITY;
-    }
+    out_logp[n] = 0.f;
+    out_lse[n] = -INFINITY;
     return;
   }
-  float M, S;
-  merge_splits_warp(p, n, lane, stage[warp][0], stage[warp][1], M, S);
-  if (lane == 0) {
-    const float ls = logf(S);
-    out_lse[n] = M + ls;
-    out_logp[n] = (p.zt[n] - M) - ls;
-  }
+  const float ls = logf(S);
+  out_lse[n] = M + ls;
+  out_logp[n] = (p.zt[n] - M) - ls;
 }
 
 // Vocab-parallel shard statistics ("Fused Linear LogP", Tensor Parallel Vocab
@@ -220,21 +229,17 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __re
 // else -inf.
 __global__ void __launch_bounds__(256) shard_stats_kernel(FwdParams p, float* __restrict__ out_max,
                                                           float* __restrict__ out_se, float* __restrict__ out_tl) {
-  __shared__ float stage[kMergeWarps][2][kMergeChunk];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * kMergeWarps + warp;
-  if (n >= p.N) return;  // warp-uniform
+  __shared__ MergeSmem sm;
+  const int n = blockIdx.x * kMergeRows + (threadIdx.x & 31);
   float M, S;
-  merge_splits_warp(p, n, lane, stage[warp][0], stage[warp][1], M, S);
-  if (lane == 0) {
-    const long long t = p.targets[n];
-    const long long tl = t - p.vocab_start;
-    const bool local = t != p.ignore_index && tl >= 0 && tl < static_cast<long long>(p.V);
-    out_max[n] = M;
-    out_se[n] = S;
-    out_tl[n] = local ? p.zt[n] : -INFINITY;
-  }
+  merge_splits_block(p, n, sm, M, S);
+  if (threadIdx.x >= 32 || n >= p.N) return;
+  const long long t = p.targets[n];
+  const long long tl = t - p.vocab_start;
+  const bool local = t != p.ignore_index && tl >= 0 && tl < static_cast<long long>(p.V);
+  out_max[n] = M;
+  out_se[n] = S;
+  out_tl[n] = local ? p.zt[n] : -INFINITY;
 }
 
 // Merge of R shards' (max, sum, target logit) in ascending rank order, then the
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(256) merge_shards_kernel(const float* __restri
 
 cudaError_t launch_shard_stats(const FwdParams& p, float* out_max, float* out_sumexp, float* out_tlogit,
                                cudaStream_t s) {
-  shard_stats_kernel<<<(p.N + kMergeWarps - 1) / kMergeWarps, 256, 0, s>>>(p, out_max, out_sumexp, out_tlogit);
+  shard_stats_kernel<<<(p.N + kMergeRows - 1) / kMergeRows, 256, 0, s>>>(p, out_max, out_sumexp, out_tlogit);
   return cudaGetLastError();
 }
 
@@ -302,7 +307,7 @@ cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w
 }
 
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s) {
-  fwd_merge_kernel<<<(p.N + kMergeWarps - 1) / kMergeWarps, 256, 0, s>>>(p, out_logp, out_lse);
+  fwd_merge_kernel<<<(p.N + kMergeRows - 1) / kMergeRows, 256, 0, s>>>(p, out_logp, out_lse);
   return cudaGetLastError();
 }
 

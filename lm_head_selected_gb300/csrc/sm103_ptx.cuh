@@ -39,6 +39,19 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// 2^x with the hardware's approximate exp2 instruction (PTX ex2.approx.ftz:
+// subnormal results flush to zero), one instruction per call.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+#ifndef LLP_EPI_FASTEXP
+#define LLP_EPI_FASTEXP 1  // GEMM epilogues: ex2.approx.ftz instead of exp2f
+#endif
+__device__ __forceinline__ float epi_exp2(float x) { return LLP_EPI_FASTEXP ? ex2_approx(x) : exp2f(x); }
+
 // ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
