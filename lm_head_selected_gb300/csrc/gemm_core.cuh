@@ -49,6 +49,9 @@
 
 namespace llp {
 
+// exp2 of the epilogues' softmax terms
+__device__ __forceinline__ float epi_exp2(float x) { return LLP_EPI_FASTEXP ? ex2_approx(x) : exp2f(x); }
+
 constexpr int BM = kTileM;  // accumulator rows per CTA
 constexpr int BK = kTileK;
 constexpr int UMMA_K = 16;
@@ -409,7 +412,9 @@ __device__ __forceinline__ void run_epilogue(const SharedState& st, const CUtens
       __syncwarp();
       if (lane == 0) {
         if (P::PAIR)
-          LLP_TMEM_RELEASE(map_to_cta(smem_u32(&st.tmem_empty[buf]), 0));
+          // CTA-scope arrive: the tcgen05 fence above orders the TMEM reads; a
+          // cluster-scope release here was the top stall of short-unit launches
+          mbar_arrive_remote(map_to_cta(smem_u32(&st.tmem_empty[buf]), 0));
         else
           mbar_arrive(&st.tmem_empty[buf]);
       }

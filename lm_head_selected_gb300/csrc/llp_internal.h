@@ -36,13 +36,13 @@ constexpr int kPairStages = LLP_PAIR_STAGES;
 #ifndef LLP_DZ_STREAM
 #define LLP_DZ_STREAM 1      // store the bf16 dlogits with L2 evict-first priority
 #endif
-#ifndef LLP_TMEM_RELEASE
-#define LLP_TMEM_RELEASE mbar_arrive_remote
-#endif
 #ifndef LLP_DYN_MIN_KB
 #define LLP_DYN_MIN_KB 128   // in-order claiming only for units of at least this many k-blocks
 #endif
 constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
+#ifndef LLP_EPI_FASTEXP
+#define LLP_EPI_FASTEXP 1    // GEMM epilogues: the ex2.approx.ftz instruction instead of exp2f
+#endif
 #ifndef LLP_HALF_TILE
 #define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
 #endif

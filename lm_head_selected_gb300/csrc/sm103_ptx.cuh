@@ -47,11 +47,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-#ifndef LLP_EPI_FASTEXP
-#define LLP_EPI_FASTEXP 1  // GEMM epilogues: ex2.approx.ftz instead of exp2f
-#endif
-__device__ __forceinline__ float epi_exp2(float x) { return LLP_EPI_FASTEXP ? ex2_approx(x) : exp2f(x); }
-
 // ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
