@@ -47,6 +47,13 @@ WORKLOADS = {
     "nemotron_n32": (32, 2688, 131072,
                      "Nemotron-3-Nano LM head, N=32 (2x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
                      "uniform targets, grad_logp=1"),
+    # the training-step and long-context parity configurations, timed for reference
+    "train_d4096": (16384, 4096, 128256,
+                    "training step, N=16384, D=4096, V=128256, bf16, bias~N(0,0.1^2), grad_logp~N(0,1), "
+                    "uniform targets"),
+    "long_context": (65600, 2688, 131072,
+                     "long-context stress, N=65600, D=2688, V=131072, no bias, one row shifted by +9984, "
+                     "duplicate targets; grad_weight reduced over three 32768-token segments"),
 }
 # The pages' number for this metric and workload: strict fused fwd+bwd, 16384 tokens,
 # D=2688, V=131072, 351.2 ms on an H100 PCIe ("Feat/nemotron h lm head logprob cuda",
@@ -184,6 +191,12 @@ def make_workload(name):
     N, D, V, desc = WORKLOADS[name]
     if name == "nemotron_n32":
         inp = workloads.nemotron_head(N=N, seed=1001)
+    elif name == "train_d4096":
+        inp = workloads.train(N=N, seed=1003)
+    elif name == "long_context":
+        inp = workloads.long_context(N=N, seed=1004)
+        import torch
+        inp.grad_logp = torch.randn(N, generator=torch.Generator().manual_seed(1004))
     else:
         inp = workloads.rl_scoring(N=N, D=D, V=V, seed=1002, grad_std=1.0)
     return inp, desc
