@@ -280,11 +280,12 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   return LLP_OK;
 }
 
-// K-blocks of a gradient GEMM's shortest unit (its last K segment).
-int64_t min_units_kblocks(const llp::GradGemmParams& p) {
+// K-blocks of a gradient GEMM's longest unit (a full K segment, or all of K
+// when it is shorter).  The long units carry the work and the L2 reuse that
+// in-order claiming protects; a short last segment rides along.
+int64_t max_unit_kblocks(const llp::GradGemmParams& p) {
   const int64_t total = cdiv(p.K, llp::kTileK);
-  const int64_t rest = total - static_cast<int64_t>(p.nseg - 1) * p.kseg_blocks;
-  return rest < p.kseg_blocks ? rest : p.kseg_blocks;
+  return total < p.kseg_blocks ? total : p.kseg_blocks;
 }
 
 // Backward launch sequence on validated arguments (N > 0, workspace sized by bwd_layout).
@@ -356,7 +357,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.err = dev->status_ptr;
     p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
     p.f16 = f16 ? 1 : 0;
-    p.sched = min_units_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
+    p.sched = max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
     if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
@@ -391,7 +392,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.f32_out = 0;
     p.f16 = f16 ? 1 : 0;
     p.err = dev->status_ptr;
-    p.sched = min_units_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
+    p.sched = max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
     if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;

@@ -37,7 +37,7 @@ constexpr int kPairStages = LLP_PAIR_STAGES;
 #define LLP_DZ_STREAM 1      // store the bf16 dlogits with L2 evict-first priority
 #endif
 #ifndef LLP_DYN_MIN_KB
-#define LLP_DYN_MIN_KB 128   // in-order claiming only for units of at least this many k-blocks
+#define LLP_DYN_MIN_KB 128   // in-order claiming only when full units span at least this many k-blocks
 #endif
 constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 #ifndef LLP_EPI_FASTEXP
