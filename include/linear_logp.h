@@ -70,6 +70,13 @@ enum {
   LLP_ERR_SCRATCH_LIMIT = -8        /* problem too large for linear_logp_fwd_noalloc's fixed scratch */
 };
 
+/* Scheduling note: the gradient GEMMs hand out their work units in ascending
+ * order from a counter in the backward workspace when the units are long, and
+ * round-robin otherwise.  Which SM computes a unit never changes the
+ * arithmetic, so results are bitwise the same either way; setting the
+ * environment variable LINEAR_LOGP_SCHEDULE=static before the library's first
+ * call forces round-robin everywhere (a diagnostic, read once per process). */
+
 /* Bytes of workspace linear_logp_fwd needs for an N x D x V problem
  * (0 when N == 0).  The workspace holds the per-vocab-split (max, sum) pairs
  * and the captured target logits. */

@@ -3,6 +3,8 @@
 // Declarations and the contract are in include/linear_logp.h.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -280,6 +282,16 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   return LLP_OK;
 }
 
+// LINEAR_LOGP_SCHEDULE=static (read once per process) makes every GEMM take its
+// units round-robin.  A diagnostic: results are the same under either schedule.
+bool force_static_schedule() {
+  static const bool v = [] {
+    const char* e = std::getenv("LINEAR_LOGP_SCHEDULE");
+    return e != nullptr && std::strcmp(e, "static") == 0;
+  }();
+  return v;
+}
+
 // K-blocks of a gradient GEMM's longest unit (a full K segment, or all of K
 // when it is shorter).  The long units carry the work and the L2 reuse that
 // in-order claiming protects; a short last segment rides along.
@@ -357,7 +369,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.err = dev->status_ptr;
     p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
     p.f16 = f16 ? 1 : 0;
-    p.sched = max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
+    p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
     if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
@@ -392,7 +404,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.f32_out = 0;
     p.f16 = f16 ? 1 : 0;
     p.err = dev->status_ptr;
-    p.sched = max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
+    p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
     if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;

@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "llp_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace llp {
 
@@ -30,13 +31,7 @@ constexpr float kLog2eL = 1.4426950408889634f;
 constexpr int kLChunk = 4;
 constexpr int kLMinBlocks = 8;
 
-// 2^x with the hardware's approximate exp2 (subnormal results flush to zero),
-// one instruction; its relative error is far below bf16 resolution.
-__device__ __forceinline__ float ex2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+
 
 __device__ __forceinline__ bool tgt_ok(long long t, int V, long long ignore_index) {
   return t != ignore_index && t >= 0 && t < static_cast<long long>(V);
@@ -204,7 +199,7 @@ __global__ void __launch_bounds__(kLThreads, kLMinBlocks) logits_split_kernel(co
       float x[W];
       VV::unpack(raw[i], x);
 #pragma unroll
-      for (int k = 0; k < W; ++k) cs += ex2_ftz((x[k] - cm) * kLog2eL);
+      for (int k = 0; k < W; ++k) cs += ex2_approx((x[k] - cm) * kLog2eL);
     }
     merge_ms(m, s, cm, cs);
   }
@@ -280,7 +275,7 @@ __global__ void __launch_bounds__(kLThreads) logits_grad_kernel(const typename V
     }
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-      const float p = ex2_ftz(((x[k] - m) - ls) * kLog2eL);
+      const float p = ex2_approx(((x[k] - m) - ls) * kLog2eL);
       const float oh = (static_cast<long long>(v + k) == t) ? 1.f : 0.f;
       x[k] = ok ? g * (oh - p) : 0.f;
     }
