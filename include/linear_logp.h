@@ -163,7 +163,8 @@ int linear_logp_bwd(const float* grad_logp, const float* saved_lse, const void* 
  * product have one type; every accumulation stays fp32.  fp16 cannot hold a
  * dlogit above 65504 in magnitude: |grad_logp / temperature| must stay below
  * that.  fp32 inputs are not accepted by any entry point (the Python wrapper
- * refuses them).
+ * refuses them).  The row-subset variants have fp16 forms too
+ * (linear_logp_fwd_indexed_f16 / linear_logp_bwd_indexed_f16).
  */
 int linear_logp_fwd_f16(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
                         const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
@@ -199,6 +200,17 @@ int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, cons
                             int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
                             void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
                             size_t workspace_bytes, void* stream);
+/* fp16 forms of the two row-subset variants: IEEE fp16 hidden / weight /
+ * grad_hidden / grad_weight, otherwise as above (see linear_logp_fwd_f16). */
+int linear_logp_fwd_indexed_f16(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                                const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                                const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+int linear_logp_bwd_indexed_f16(const float* grad_logp, const float* saved_lse, const void* hidden,
+                                const void* weight, const float* bias, const int64_t* targets,
+                                const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                                const int64_t* indices, int64_t K, void* grad_hidden, void* grad_weight,
+                                float* grad_bias, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Vocab-parallel shards ("Fused Linear LogP", Tensor Parallel Vocab Shards: each

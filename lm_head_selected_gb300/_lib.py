@@ -42,6 +42,8 @@ EXPORTED = (
     "linear_logp_sum_partials",
     "linear_logp_fwd_f16",
     "linear_logp_bwd_f16",
+    "linear_logp_fwd_indexed_f16",
+    "linear_logp_bwd_indexed_f16",
 )
 # include/fused_logp.h (logits-input op, same library)
 EXPORTED_FUSED = (
@@ -122,6 +124,10 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_bwd_indexed.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p, _i64, _p,
                                                 _p, _p, _p, _size, _p]
         lib.linear_logp_bwd_indexed.restype = ctypes.c_int
+        lib.linear_logp_fwd_indexed_f16.argtypes = lib.linear_logp_fwd_indexed.argtypes
+        lib.linear_logp_fwd_indexed_f16.restype = ctypes.c_int
+        lib.linear_logp_bwd_indexed_f16.argtypes = lib.linear_logp_bwd_indexed.argtypes
+        lib.linear_logp_bwd_indexed_f16.restype = ctypes.c_int
         lib.linear_logp_fwd_shard.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p,
                                               _size, _p]
         lib.linear_logp_fwd_shard.restype = ctypes.c_int

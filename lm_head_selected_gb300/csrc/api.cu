@@ -591,10 +591,11 @@ size_t linear_logp_bwd_indexed_workspace_bytes(int64_t N, int64_t D, int64_t V, 
   return idx_layout(N, D, V, K, true, has_bias != 0).total;
 }
 
-int linear_logp_fwd_indexed(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
-                            const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
-                            const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+// hidden / weight bf16, or IEEE fp16 when f16 (the row copies move raw 16-bit values).
+static int fwd_indexed_entry(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                             const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                             const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
+                             size_t workspace_bytes, void* stream, bool f16) {
   int st = check_shapes(N, D, V);
   if (st != LLP_OK) return st;
   if (K < 0 || K > kLim31) return LLP_ERR_BAD_SHAPE;
@@ -626,17 +627,33 @@ int linear_logp_fwd_indexed(const void* hidden, const void* weight, const float*
   float* c_logp = reinterpret_cast<float*>(ws + L.c_a);
   float* c_lse = reinterpret_cast<float*>(ws + L.c_b);
   st = fwd_core(dev, c_hidden, weight, bias, reinterpret_cast<const int64_t*>(c_targets), c_temp, L.Kc, D, V,
-                ignore_index, c_logp, c_lse, ws + L.inner, s);
+                ignore_index, c_logp, c_lse, ws + L.inner, s, 0, nullptr, nullptr, nullptr, f16);
   if (st != LLP_OK) return st;
   return llp::scatter_selected_outputs(sel, c_logp, c_lse, out_logp, out_lse, s) == cudaSuccess ? LLP_OK
                                                                                                 : LLP_ERR_CUDA;
 }
 
-int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
-                            const float* bias, const int64_t* targets, const float* temperature, int64_t N,
-                            int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
-                            void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
+int linear_logp_fwd_indexed(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                            const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                            const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
                             size_t workspace_bytes, void* stream) {
+  return fwd_indexed_entry(hidden, weight, bias, targets, temperature, N, D, V, ignore_index, indices, K, out_logp,
+                           out_lse, workspace, workspace_bytes, stream, false);
+}
+
+int linear_logp_fwd_indexed_f16(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
+                                const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                                const int64_t* indices, int64_t K, float* out_logp, float* out_lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return fwd_indexed_entry(hidden, weight, bias, targets, temperature, N, D, V, ignore_index, indices, K, out_logp,
+                           out_lse, workspace, workspace_bytes, stream, true);
+}
+
+static int bwd_indexed_entry(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                             const float* bias, const int64_t* targets, const float* temperature, int64_t N,
+                             int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
+                             void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
+                             size_t workspace_bytes, void* stream, bool f16) {
   int st = check_shapes(N, D, V);
   if (st != LLP_OK) return st;
   if (K < 0 || K > kLim31) return LLP_ERR_BAD_SHAPE;
@@ -683,13 +700,31 @@ int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, cons
     return LLP_ERR_CUDA;
   auto* c_gh = grad_hidden ? reinterpret_cast<__nv_bfloat16*>(ws + L.c_gh) : nullptr;
   st = bwd_core(dev, c_grad, c_lse, c_hidden, weight, bias, reinterpret_cast<const int64_t*>(c_targets), c_temp,
-                L.Kc, D, V, ignore_index, c_gh, grad_weight, grad_bias, ws + L.inner, s);
+                L.Kc, D, V, ignore_index, c_gh, grad_weight, grad_bias, ws + L.inner, s, 0, -1, nullptr, f16);
   if (st != LLP_OK) return st;
   if (grad_hidden &&
       llp::scatter_selected_grad_hidden(sel, static_cast<int>(N), static_cast<int>(D), c_gh,
                                         static_cast<__nv_bfloat16*>(grad_hidden), s) != cudaSuccess)
     return LLP_ERR_CUDA;
   return LLP_OK;
+}
+
+int linear_logp_bwd_indexed(const float* grad_logp, const float* saved_lse, const void* hidden, const void* weight,
+                            const float* bias, const int64_t* targets, const float* temperature, int64_t N,
+                            int64_t D, int64_t V, int64_t ignore_index, const int64_t* indices, int64_t K,
+                            void* grad_hidden, void* grad_weight, float* grad_bias, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return bwd_indexed_entry(grad_logp, saved_lse, hidden, weight, bias, targets, temperature, N, D, V, ignore_index,
+                           indices, K, grad_hidden, grad_weight, grad_bias, workspace, workspace_bytes, stream, false);
+}
+
+int linear_logp_bwd_indexed_f16(const float* grad_logp, const float* saved_lse, const void* hidden,
+                                const void* weight, const float* bias, const int64_t* targets,
+                                const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                                const int64_t* indices, int64_t K, void* grad_hidden, void* grad_weight,
+                                float* grad_bias, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_indexed_entry(grad_logp, saved_lse, hidden, weight, bias, targets, temperature, N, D, V, ignore_index,
+                           indices, K, grad_hidden, grad_weight, grad_bias, workspace, workspace_bytes, stream, true);
 }
 
 // ----------------------------------------------------------------------------

@@ -3,7 +3,7 @@
 PyTorch supplies device memory and the current stream; every step of the
 computation runs in the CUDA kernels of ``liblinear_logp.so``.  Inputs are
 checked here and rejected (no fallback, no casting): hidden/weight bf16 (or
-both fp16 for the plain forward / backward and ``linear_logp``),
+both fp16 for the plain and row-subset forward / backward and ``linear_logp``),
 bias/temperature/grad fp32, targets int64, all contiguous on one CUDA device.
 
 Entry points mirror the C ABI names:
@@ -169,8 +169,9 @@ def linear_logp_fwd_indexed(hidden: torch.Tensor, weight: torch.Tensor, targets:
                             out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
     """Forward on the rows named by ``indices`` only (duplicates count once, out of
     range ignored).  Selected rows of ``out`` get the plain forward's values; the
-    others keep their contents (new buffers start as logp 0 / lse -inf)."""
-    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    others keep their contents (new buffers start as logp 0 / lse -inf).  hidden /
+    weight are both bf16 or both fp16."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature, allow_f16=True)
     idx = _check_indices(indices, dev)
     lib = _lib.load()
     if out is None:
@@ -180,10 +181,11 @@ def linear_logp_fwd_indexed(hidden: torch.Tensor, weight: torch.Tensor, targets:
         logp, lse = out
     K = idx.numel()
     ws = _workspace(int(lib.linear_logp_fwd_indexed_workspace_bytes(N, D, V, K)), dev, None)
-    st = lib.linear_logp_fwd_indexed(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), _ptr(temperature),
-                                     N, D, V, int(ignore_index), _ptr(idx), K, _ptr(logp), _ptr(lse), _ptr(ws),
-                                     ws.numel(), _stream(dev))
-    _lib.check("linear_logp_fwd_indexed", st)
+    name = "linear_logp_fwd_indexed_f16" if hidden.dtype == torch.float16 else "linear_logp_fwd_indexed"
+    st = getattr(lib, name)(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), _ptr(temperature),
+                            N, D, V, int(ignore_index), _ptr(idx), K, _ptr(logp), _ptr(lse), _ptr(ws),
+                            ws.numel(), _stream(dev))
+    _lib.check(name, st)
     return logp, lse
 
 
@@ -193,21 +195,22 @@ def linear_logp_bwd_indexed(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hi
                             ignore_index: int = IGNORE_INDEX, need_hidden: bool = True, need_weight: bool = True,
                             need_bias: bool = True):
     """Gradients of the sum over the selected rows of grad_logp * logp; grad_hidden
-    rows that are not selected are zero."""
-    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature)
+    rows that are not selected are zero; 16-bit gradients in the inputs' dtype."""
+    dev, N, D, V = _check_inputs(hidden, weight, targets, bias, temperature, allow_f16=True)
     idx = _check_indices(indices, dev)
     _need(grad_logp, "grad_logp", torch.float32, dev, 1)
     _need(saved_lse, "saved_lse", torch.float32, dev, 1)
     lib = _lib.load()
-    gh = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if need_hidden else None
-    gw = torch.empty((V, D), dtype=torch.bfloat16, device=dev) if need_weight else None
+    gh = torch.empty((N, D), dtype=hidden.dtype, device=dev) if need_hidden else None
+    gw = torch.empty((V, D), dtype=hidden.dtype, device=dev) if need_weight else None
     gb = torch.empty(V, dtype=torch.float32, device=dev) if (need_bias and bias is not None) else None
     K = idx.numel()
     ws = _workspace(int(lib.linear_logp_bwd_indexed_workspace_bytes(N, D, V, K, int(bias is not None))), dev, None)
-    st = lib.linear_logp_bwd_indexed(_ptr(grad_logp), _ptr(saved_lse), _ptr(hidden), _ptr(weight), _ptr(bias),
-                                     _ptr(targets), _ptr(temperature), N, D, V, int(ignore_index), _ptr(idx), K,
-                                     _ptr(gh), _ptr(gw), _ptr(gb), _ptr(ws), ws.numel(), _stream(dev))
-    _lib.check("linear_logp_bwd_indexed", st)
+    name = "linear_logp_bwd_indexed_f16" if hidden.dtype == torch.float16 else "linear_logp_bwd_indexed"
+    st = getattr(lib, name)(_ptr(grad_logp), _ptr(saved_lse), _ptr(hidden), _ptr(weight), _ptr(bias),
+                            _ptr(targets), _ptr(temperature), N, D, V, int(ignore_index), _ptr(idx), K,
+                            _ptr(gh), _ptr(gw), _ptr(gb), _ptr(ws), ws.numel(), _stream(dev))
+    _lib.check(name, st)
     return gh, gw, gb
 
 

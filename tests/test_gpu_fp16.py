@@ -93,6 +93,35 @@ def test_mixed_or_fp32_inputs_are_refused():
         llp.linear_logp_fwd(h, torch.zeros(10, 64, device="cuda", dtype=torch.bfloat16), t)
     with pytest.raises(TypeError):
         llp.linear_logp_fwd(h.float(), torch.zeros(10, 64, device="cuda"), t)
-    with pytest.raises(TypeError):  # the row-subset variants stay bf16-only
-        llp.linear_logp_fwd_indexed(h, torch.zeros(10, 64, device="cuda", dtype=torch.float16), t,
-                                    torch.zeros(1, dtype=torch.int64, device="cuda"))
+    with pytest.raises(TypeError):  # the no-allocation forward stays bf16-only
+        llp.ops.linear_logp_fwd_noalloc(h, torch.zeros(10, 64, device="cuda", dtype=torch.float16), t)
+
+
+def test_fp16_row_subsets():
+    """fp16 row-subset forward gives the plain fp16 forward's values on the selected
+    rows; its backward matches the oracle restricted to those rows."""
+    import numpy as np
+
+    import lm_head_selected_gb300 as llp
+    import oracle
+    from parity_helpers import GH_ATOL, GH_RTOL, GW_ATOL, GW_RTOL, assert_close, oracle_args
+    inp = workloads.make_inputs(300, 192, 1500, seed=23, weight_std=0.15, bias_std=0.3, n_ignore=4, grad_std=1.0,
+                                dtype=torch.float16)
+    d = to_device(inp)
+    idx = torch.tensor([5, 17, 17, 250, 299, 0, 1000, -3], dtype=torch.int64, device="cuda")
+    rows = sorted({5, 17, 250, 299, 0})
+    lp_all, lse_all = gpu_fwd(d)
+    lp, lse = llp.linear_logp_fwd_indexed(d["hidden"], d["weight"], d["targets"], idx, d["bias"])
+    r = torch.tensor(rows, device="cuda")
+    assert torch.equal(lp[r], lp_all[r]) and torch.equal(lse[r], lse_all[r])
+    gh, gw, gb = llp.linear_logp_bwd_indexed(d["grad_logp"], lse_all, d["hidden"], d["weight"], d["targets"], idx,
+                                             d["bias"])
+    check_device_status()
+    assert gh.dtype == torch.float16 and gw.dtype == torch.float16
+    sub = inp.rows(torch.tensor(rows))
+    gh_ref, gw_ref, gb_ref = oracle.backward(np64(sub.grad_logp), *oracle_args(sub))
+    assert_close("grad_hidden[rows]", np64(gh)[rows], gh_ref, GH_ATOL, GH_RTOL)
+    others = np.setdiff1d(np.arange(inp.N), rows)
+    assert np.all(np64(gh)[others] == 0)
+    assert_close("grad_weight", np64(gw), gw_ref, GW_ATOL, GW_RTOL)
+    assert_close("grad_bias", np64(gb), gb_ref, GW_ATOL, GW_RTOL)
