@@ -247,6 +247,21 @@ int linear_logp_bwd_shard(const float* grad_logp, const float* lse, const void* 
                           float* grad_hidden_partial, void* grad_weight_local, float* grad_bias_local,
                           void* workspace, size_t workspace_bytes, void* stream);
 int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream);
+/* fp16 forms of the shard entry points: hidden / weight_local /
+ * grad_weight_local in IEEE fp16 and an fp16 sum of the partials; otherwise as
+ * above (see linear_logp_fwd_f16). */
+int linear_logp_fwd_shard_f16(const void* hidden, const void* weight_local, const float* bias_local,
+                              const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                              int64_t V_local, int64_t vocab_start, int64_t ignore_index, float* out_max,
+                              float* out_sumexp, float* out_target_logit, void* workspace, size_t workspace_bytes,
+                              void* stream);
+int linear_logp_bwd_shard_f16(const float* grad_logp, const float* lse, const void* hidden,
+                              const void* weight_local, const float* bias_local, const int64_t* targets,
+                              const float* temperature, int64_t N, int64_t D, int64_t V_local, int64_t vocab_start,
+                              int64_t global_V, int64_t ignore_index, float* grad_hidden_partial,
+                              void* grad_weight_local, float* grad_bias_local, void* workspace,
+                              size_t workspace_bytes, void* stream);
+int linear_logp_sum_partials_f16(const float* parts, int64_t R, int64_t count, void* out_f16, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* linear_logp_status_string(int status);

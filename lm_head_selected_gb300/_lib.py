@@ -44,6 +44,9 @@ EXPORTED = (
     "linear_logp_bwd_f16",
     "linear_logp_fwd_indexed_f16",
     "linear_logp_bwd_indexed_f16",
+    "linear_logp_fwd_shard_f16",
+    "linear_logp_bwd_shard_f16",
+    "linear_logp_sum_partials_f16",
 )
 # include/fused_logp.h (logits-input op, same library)
 EXPORTED_FUSED = (
@@ -138,6 +141,10 @@ def load() -> ctypes.CDLL:
         lib.linear_logp_bwd_shard.restype = ctypes.c_int
         lib.linear_logp_sum_partials.argtypes = [_p, _i64, _i64, _p, _p]
         lib.linear_logp_sum_partials.restype = ctypes.c_int
+        for name in ("fwd_shard", "bwd_shard", "sum_partials"):
+            f16, base = getattr(lib, f"linear_logp_{name}_f16"), getattr(lib, f"linear_logp_{name}")
+            f16.argtypes = base.argtypes
+            f16.restype = ctypes.c_int
         lib.fused_logp_workspace_bytes.argtypes = [_i64, _i64]
         lib.fused_logp_workspace_bytes.restype = _size
         lib.fused_logp_fwd.argtypes = [_p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _p, _p, _p, _size, _p]

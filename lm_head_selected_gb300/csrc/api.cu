@@ -730,10 +730,11 @@ int linear_logp_bwd_indexed_f16(const float* grad_logp, const float* saved_lse, 
 // ----------------------------------------------------------------------------
 // Vocab-parallel shards.
 // ----------------------------------------------------------------------------
-int linear_logp_fwd_shard(const void* hidden, const void* weight_local, const float* bias_local,
-                          const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V_local,
-                          int64_t vocab_start, int64_t ignore_index, float* out_max, float* out_sumexp,
-                          float* out_target_logit, void* workspace, size_t workspace_bytes, void* stream) {
+// hidden / weight_local bf16, or IEEE fp16 when f16.
+static int fwd_shard_entry(const void* hidden, const void* weight_local, const float* bias_local,
+                           const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V_local,
+                           int64_t vocab_start, int64_t ignore_index, float* out_max, float* out_sumexp,
+                           float* out_target_logit, void* workspace, size_t workspace_bytes, void* stream, bool f16) {
   int st = check_shapes(N, D, V_local);
   if (st != LLP_OK) return st;
   if (vocab_start < 0 || vocab_start > kLim31 - V_local) return LLP_ERR_BAD_SHAPE;
@@ -750,7 +751,26 @@ int linear_logp_fwd_shard(const void* hidden, const void* weight_local, const fl
   if ((st = load_encode_fn()) != LLP_OK) return st;
   return fwd_core(dev, hidden, weight_local, bias_local, targets, temperature, N, D, V_local, ignore_index, nullptr,
                   nullptr, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream), vocab_start, out_max,
-                  out_sumexp, out_target_logit);
+                  out_sumexp, out_target_logit, f16);
+}
+
+int linear_logp_fwd_shard(const void* hidden, const void* weight_local, const float* bias_local,
+                          const int64_t* targets, const float* temperature, int64_t N, int64_t D, int64_t V_local,
+                          int64_t vocab_start, int64_t ignore_index, float* out_max, float* out_sumexp,
+                          float* out_target_logit, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_shard_entry(hidden, weight_local, bias_local, targets, temperature, N, D, V_local, vocab_start,
+                         ignore_index, out_max, out_sumexp, out_target_logit, workspace, workspace_bytes, stream,
+                         false);
+}
+
+int linear_logp_fwd_shard_f16(const void* hidden, const void* weight_local, const float* bias_local,
+                              const int64_t* targets, const float* temperature, int64_t N, int64_t D,
+                              int64_t V_local, int64_t vocab_start, int64_t ignore_index, float* out_max,
+                              float* out_sumexp, float* out_target_logit, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return fwd_shard_entry(hidden, weight_local, bias_local, targets, temperature, N, D, V_local, vocab_start,
+                         ignore_index, out_max, out_sumexp, out_target_logit, workspace, workspace_bytes, stream,
+                         true);
 }
 
 int linear_logp_merge_shards(const float* shard_max, const float* shard_sumexp, const float* shard_target_logit,
@@ -774,11 +794,11 @@ int linear_logp_merge_shards(const float* shard_max, const float* shard_sumexp, 
              : LLP_ERR_CUDA;
 }
 
-int linear_logp_bwd_shard(const float* grad_logp, const float* lse, const void* hidden, const void* weight_local,
-                          const float* bias_local, const int64_t* targets, const float* temperature, int64_t N,
-                          int64_t D, int64_t V_local, int64_t vocab_start, int64_t global_V, int64_t ignore_index,
-                          float* grad_hidden_partial, void* grad_weight_local, float* grad_bias_local,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+static int bwd_shard_entry(const float* grad_logp, const float* lse, const void* hidden, const void* weight_local,
+                           const float* bias_local, const int64_t* targets, const float* temperature, int64_t N,
+                           int64_t D, int64_t V_local, int64_t vocab_start, int64_t global_V, int64_t ignore_index,
+                           float* grad_hidden_partial, void* grad_weight_local, float* grad_bias_local,
+                           void* workspace, size_t workspace_bytes, void* stream, bool f16) {
   int st = check_shapes(N, D, V_local);
   if (st != LLP_OK) return st;
   if (vocab_start < 0 || global_V < 1 || global_V > kLim31 || vocab_start > global_V - V_local)
@@ -809,10 +829,32 @@ int linear_logp_bwd_shard(const float* grad_logp, const float* lse, const void* 
   if ((st = load_encode_fn()) != LLP_OK) return st;
   return bwd_core(dev, grad_logp, lse, hidden, weight_local, bias_local, targets, temperature, N, D, V_local,
                   ignore_index, nullptr, grad_weight_local, grad_bias_local, static_cast<uint8_t*>(workspace), s,
-                  vocab_start, global_V, grad_hidden_partial);
+                  vocab_start, global_V, grad_hidden_partial, f16);
 }
 
-int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream) {
+int linear_logp_bwd_shard(const float* grad_logp, const float* lse, const void* hidden, const void* weight_local,
+                          const float* bias_local, const int64_t* targets, const float* temperature, int64_t N,
+                          int64_t D, int64_t V_local, int64_t vocab_start, int64_t global_V, int64_t ignore_index,
+                          float* grad_hidden_partial, void* grad_weight_local, float* grad_bias_local,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_shard_entry(grad_logp, lse, hidden, weight_local, bias_local, targets, temperature, N, D, V_local,
+                         vocab_start, global_V, ignore_index, grad_hidden_partial, grad_weight_local,
+                         grad_bias_local, workspace, workspace_bytes, stream, false);
+}
+
+int linear_logp_bwd_shard_f16(const float* grad_logp, const float* lse, const void* hidden,
+                              const void* weight_local, const float* bias_local, const int64_t* targets,
+                              const float* temperature, int64_t N, int64_t D, int64_t V_local, int64_t vocab_start,
+                              int64_t global_V, int64_t ignore_index, float* grad_hidden_partial,
+                              void* grad_weight_local, float* grad_bias_local, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return bwd_shard_entry(grad_logp, lse, hidden, weight_local, bias_local, targets, temperature, N, D, V_local,
+                         vocab_start, global_V, ignore_index, grad_hidden_partial, grad_weight_local,
+                         grad_bias_local, workspace, workspace_bytes, stream, true);
+}
+
+static int sum_partials_entry(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream,
+                              bool f16) {
   if (R < 1 || count < 0 || (count % 4) != 0 || !product_ok(R, count)) return LLP_ERR_BAD_SHAPE;
   if (count == 0) return LLP_OK;
   if (parts == nullptr || out_bf16 == nullptr) return LLP_ERR_NULL_POINTER;
@@ -821,9 +863,17 @@ int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void*
   const int st = init_device(&dev);
   if (st != LLP_OK) return st;
   return llp::launch_segment_sum(parts, static_cast<int>(R), count, static_cast<__nv_bfloat16*>(out_bf16),
-                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+                                 static_cast<cudaStream_t>(stream), f16 ? 1 : 0) == cudaSuccess
              ? LLP_OK
              : LLP_ERR_CUDA;
+}
+
+int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream) {
+  return sum_partials_entry(parts, R, count, out_bf16, stream, false);
+}
+
+int linear_logp_sum_partials_f16(const float* parts, int64_t R, int64_t count, void* out_f16, void* stream) {
+  return sum_partials_entry(parts, R, count, out_f16, stream, true);
 }
 
 // ----------------------------------------------------------------------------

@@ -31,15 +31,17 @@ from .ops import IGNORE_INDEX, _check_inputs, _need, _ptr, _stream, _workspace
 
 def fwd_shard(hidden, weight_local, targets, vocab_start, bias_local=None, temperature=None,
               ignore_index=IGNORE_INDEX):
-    """-> stats fp32 [3, N]: (max, sum of exp(z - max), target logit or -inf) of this shard."""
-    dev, N, D, V = _check_inputs(hidden, weight_local, targets, bias_local, temperature)
+    """-> stats fp32 [3, N]: (max, sum of exp(z - max), target logit or -inf) of this shard.
+    hidden / weight_local are both bf16 or both fp16."""
+    dev, N, D, V = _check_inputs(hidden, weight_local, targets, bias_local, temperature, allow_f16=True)
     lib = _lib.load()
     stats = torch.empty((3, N), dtype=torch.float32, device=dev)
     ws = _workspace(int(lib.linear_logp_fwd_workspace_bytes(N, D, V)), dev, None)
-    st = lib.linear_logp_fwd_shard(_ptr(hidden), _ptr(weight_local), _ptr(bias_local), _ptr(targets),
-                                   _ptr(temperature), N, D, V, int(vocab_start), int(ignore_index), _ptr(stats[0]),
-                                   _ptr(stats[1]), _ptr(stats[2]), _ptr(ws), ws.numel(), _stream(dev))
-    _lib.check("linear_logp_fwd_shard", st)
+    name = "linear_logp_fwd_shard_f16" if hidden.dtype == torch.float16 else "linear_logp_fwd_shard"
+    st = getattr(lib, name)(_ptr(hidden), _ptr(weight_local), _ptr(bias_local), _ptr(targets), _ptr(temperature),
+                            N, D, V, int(vocab_start), int(ignore_index), _ptr(stats[0]), _ptr(stats[1]),
+                            _ptr(stats[2]), _ptr(ws), ws.numel(), _stream(dev))
+    _lib.check(name, st)
     return stats
 
 
@@ -60,30 +62,33 @@ def merge_shards(gathered, targets, global_vocab_size, ignore_index=IGNORE_INDEX
 
 def bwd_shard(grad_logp, lse, hidden, weight_local, targets, vocab_start, global_vocab_size, bias_local=None,
               temperature=None, ignore_index=IGNORE_INDEX, need_weight=True, need_bias=True):
-    """-> (grad_hidden contribution fp32 [N, D], local grad_weight bf16, local grad_bias fp32)."""
-    dev, N, D, V = _check_inputs(hidden, weight_local, targets, bias_local, temperature)
+    """-> (grad_hidden contribution fp32 [N, D], local grad_weight in the inputs' dtype, local grad_bias fp32)."""
+    dev, N, D, V = _check_inputs(hidden, weight_local, targets, bias_local, temperature, allow_f16=True)
     _need(grad_logp, "grad_logp", torch.float32, dev, 1)
     _need(lse, "lse", torch.float32, dev, 1)
     lib = _lib.load()
     gh = torch.empty((N, D), dtype=torch.float32, device=dev)
-    gw = torch.empty((V, D), dtype=torch.bfloat16, device=dev) if need_weight else None
+    gw = torch.empty((V, D), dtype=hidden.dtype, device=dev) if need_weight else None
     gb = torch.empty(V, dtype=torch.float32, device=dev) if (need_bias and bias_local is not None) else None
     ws = _workspace(int(lib.linear_logp_bwd_workspace_bytes(N, D, V, int(bias_local is not None))), dev, None)
-    st = lib.linear_logp_bwd_shard(_ptr(grad_logp), _ptr(lse), _ptr(hidden), _ptr(weight_local), _ptr(bias_local),
-                                   _ptr(targets), _ptr(temperature), N, D, V, int(vocab_start),
-                                   int(global_vocab_size), int(ignore_index), _ptr(gh), _ptr(gw), _ptr(gb),
-                                   _ptr(ws), ws.numel(), _stream(dev))
-    _lib.check("linear_logp_bwd_shard", st)
+    name = "linear_logp_bwd_shard_f16" if hidden.dtype == torch.float16 else "linear_logp_bwd_shard"
+    st = getattr(lib, name)(_ptr(grad_logp), _ptr(lse), _ptr(hidden), _ptr(weight_local), _ptr(bias_local),
+                            _ptr(targets), _ptr(temperature), N, D, V, int(vocab_start), int(global_vocab_size),
+                            int(ignore_index), _ptr(gh), _ptr(gw), _ptr(gb), _ptr(ws), ws.numel(), _stream(dev))
+    _lib.check(name, st)
     return gh, gw, gb
 
 
-def sum_partials(parts):
-    """parts fp32 [R, ...] -> bf16 sum over R in ascending order."""
+def sum_partials(parts, dtype=torch.bfloat16):
+    """parts fp32 [R, ...] -> sum over R in ascending order, rounded once to dtype (bf16 or fp16)."""
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("sum_partials returns bf16 or fp16")
     R = parts.shape[0]
     count = parts[0].numel()
-    out = torch.empty(parts.shape[1:], dtype=torch.bfloat16, device=parts.device)
-    st = _lib.load().linear_logp_sum_partials(_ptr(parts.contiguous()), R, count, _ptr(out), _stream(parts.device))
-    _lib.check("linear_logp_sum_partials", st)
+    out = torch.empty(parts.shape[1:], dtype=dtype, device=parts.device)
+    name = "linear_logp_sum_partials_f16" if dtype == torch.float16 else "linear_logp_sum_partials"
+    st = getattr(_lib.load(), name)(_ptr(parts.contiguous()), R, count, _ptr(out), _stream(parts.device))
+    _lib.check(name, st)
     return out
 
 
@@ -122,7 +127,7 @@ class _VocabParallelLinearLogp(torch.autograd.Function):
         gh_part, gw, gb = ops.bwd_shard(grad_logp.contiguous().float(), lse, hidden, weight_local, targets,
                                         vocab_start, global_v, bias_local, temperature, ignore_index,
                                         ctx.needs_input_grad[1], ctx.needs_input_grad[2])
-        gh = ops.sum_partials(_all_gather(gh_part, group)) if ctx.needs_input_grad[0] else None
+        gh = ops.sum_partials(_all_gather(gh_part, group), hidden.dtype) if ctx.needs_input_grad[0] else None
         return gh, gw, gb, None, None, None, None, None, None, None
 
 

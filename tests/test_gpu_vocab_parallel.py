@@ -46,18 +46,20 @@ def _run_shards(inp, R):
         parts.append(gh)
         gws.append(gw)
         gbs.append(gb)
-    gh = tp.sum_partials(torch.stack(parts))
+    gh = tp.sum_partials(torch.stack(parts), d["hidden"].dtype)
     gw = torch.cat(gws)
     gb = None if d["bias"] is None else torch.cat(gbs)
     check_device_status()
     return logp, lse, gh, gw, gb
 
 
-@pytest.mark.parametrize("R", [1, 2, 3])
-def test_sharded_forward_backward_matches_oracle(R):
+@pytest.mark.parametrize("R,dtype", [(1, torch.bfloat16), (2, torch.bfloat16), (3, torch.bfloat16),
+                                     (2, torch.float16)])
+def test_sharded_forward_backward_matches_oracle(R, dtype):
     inp = workloads.make_inputs(200, 264, 5000, seed=31 + R, weight_std=2.0 / math.sqrt(264), bias_std=0.3,
-                                temperature_range=(0.7, 1.3), n_ignore=4, n_out_of_range=3, grad_std=1.0)
+                                temperature_range=(0.7, 1.3), n_ignore=4, n_out_of_range=3, grad_std=1.0, dtype=dtype)
     logp, lse, gh, gw, gb = _run_shards(inp, R)
+    assert gh.dtype == dtype and gw.dtype == dtype
     a = oracle_args(inp)
     lp_ref, lse_ref = oracle.forward(*a)
     ok = oracle.valid_rows(inp.targets.numpy(), inp.V, -100)

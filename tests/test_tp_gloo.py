@@ -68,7 +68,7 @@ def _cpu_ops():
         dz = torch.where(ok[:, None], (g.double() * inv_tau)[:, None] * (onehot - p), torch.zeros_like(p))
         return dz @ w.double(), dz.T @ hidden.double(), (dz.sum(0) if b is not None else None)
 
-    def sum_partials(parts):
+    def sum_partials(parts, dtype=None):  # kept in float64 here; dtype names the device path's rounding
         out = torch.zeros_like(parts[0])
         for r in range(parts.shape[0]):
             out = out + parts[r]
