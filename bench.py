@@ -272,6 +272,10 @@ def run_ours(args):
     import lm_head_selected_gb300 as llp
 
     inp, desc = make_workload(args.workload)
+    if args.dtype == "fp16":  # the same values rounded to fp16 (exact for these ranges)
+        inp.hidden = inp.hidden.to(torch.float16)
+        inp.weight = inp.weight.to(torch.float16)
+        desc += "; hidden / weight in fp16"
     N, D, V = inp.N, inp.D, inp.V
     h = inp.hidden.to(dev)
     w = inp.weight.to(dev)
@@ -360,7 +364,8 @@ def run_ours(args):
                 "algorithmic_per_launch": f"{dk['algorithmic_gb'] * 1e9:.4e} bytes (every operand read once, "
                                           f"every result written once)"}
     roof["traffic"] = None
-    if (NCU_TRAFFIC and NCU_TRAFFIC["workload"] == args.workload and NCU_TRAFFIC["sources_sha"] == sources_sha()
+    if (NCU_TRAFFIC and args.dtype == "bf16" and NCU_TRAFFIC["workload"] == args.workload
+            and NCU_TRAFFIC["sources_sha"] == sources_sha()
             and dom in NCU_TRAFFIC["bytes_per_launch"]):
         roof["traffic"] = NCU_TRAFFIC["bytes_per_launch"][dom]
         for k, v in NCU_TRAFFIC["bytes_per_launch"].items():
@@ -427,7 +432,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": value / PAGES_TOKENS_PER_S, "vs_baseline_context": PAGES_CONTEXT,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": "f16" if args.dtype == "fp16" else "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "N": N, "D": D, "V": V, "bias": b is not None, "temperature": tau is not None,
                        "description": desc, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (weight 704.6 MB > 129 MB), no flush"},
@@ -536,6 +541,7 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the timed oracle sample")
     ap.add_argument("--reference-rows", type=int, default=64, help="token rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=("bf16", "fp16"), default="bf16", help="hidden / weight type")
     ap.add_argument("--op", choices=("linear_logp", "fused_logp"), default="linear_logp",
                     help="linear_logp: the fused LM-head path (default); fused_logp: the logits-input op")
     ap.add_argument("--fused-n", type=int, default=16384)
