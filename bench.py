@@ -66,9 +66,9 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by hash).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "4b631b28381aa4d9",
-    "bytes_per_launch": {"fwd_partials": 1837079296 + 37159424, "dlogits": 5396595712 + 4273137920,
-                         "grad_hidden": 23727052544 + 698042880, "grad_weight": 14363210240 + 700922112},
+    "sources_sha": "a3ab69940f6dff34",
+    "bytes_per_launch": {"fwd_partials": 2639398400 + 37245952, "dlogits": 5613756160 + 4260891136,
+                         "grad_hidden": 20002212864 + 699163136, "grad_weight": 13128675072 + 698261248},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
