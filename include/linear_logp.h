@@ -304,6 +304,18 @@ int linear_logp_selftest_wait_timeout(unsigned long long limit_ns, void* stream)
  * teardown, 6 the self-test below, 7 a role waited for its next work-unit id. */
 int linear_logp_device_status(void* stream, unsigned int* device_code);
 
+/* The cudaError_t code of the last CUDA call of this library that failed on the
+ * calling thread (the cause behind an LLP_ERR_CUDA), 0 if none, and its name.
+ * Entry points clear a pending non-sticky error that an unrelated earlier CUDA
+ * call left on the calling thread, so it is not reported as theirs. */
+int linear_logp_last_cuda_error(void);
+const char* linear_logp_cuda_error_name(int code);
+/* Diagnostic detail of the calling thread's last LLP_ERR_CUDA: the CUDA error
+ * code (0 if the failing call was not a runtime call), the CUresult of a failed
+ * tensor-map encoding (0 if none), and the library source line of the check
+ * that failed.  Pointers may be NULL.  Returns LLP_OK. */
+int linear_logp_last_failure(int* cuda_error, int* driver_result, int* site);
+
 #ifdef __cplusplus
 }
 #endif

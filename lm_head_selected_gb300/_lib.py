@@ -47,6 +47,9 @@ EXPORTED = (
     "linear_logp_fwd_shard_f16",
     "linear_logp_bwd_shard_f16",
     "linear_logp_sum_partials_f16",
+    "linear_logp_last_cuda_error",
+    "linear_logp_cuda_error_name",
+    "linear_logp_last_failure",
 )
 # include/fused_logp.h (logits-input op, same library)
 EXPORTED_FUSED = (
@@ -145,6 +148,12 @@ def load() -> ctypes.CDLL:
             f16, base = getattr(lib, f"linear_logp_{name}_f16"), getattr(lib, f"linear_logp_{name}")
             f16.argtypes = base.argtypes
             f16.restype = ctypes.c_int
+        lib.linear_logp_last_cuda_error.argtypes = []
+        lib.linear_logp_last_cuda_error.restype = ctypes.c_int
+        lib.linear_logp_cuda_error_name.argtypes = [ctypes.c_int]
+        lib.linear_logp_cuda_error_name.restype = ctypes.c_char_p
+        lib.linear_logp_last_failure.argtypes = [ctypes.POINTER(ctypes.c_int)] * 3
+        lib.linear_logp_last_failure.restype = ctypes.c_int
         lib.fused_logp_workspace_bytes.argtypes = [_i64, _i64]
         lib.fused_logp_workspace_bytes.restype = _size
         lib.fused_logp_fwd.argtypes = [_p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _p, _p, _p, _size, _p]
@@ -161,7 +170,18 @@ def status_string(status: int) -> str:
 
 def check(fn: str, status: int) -> None:
     if status != LLP_OK:
-        raise LinearLogpError(fn, status, status_string(status))
+        msg = status_string(status)
+        if status == LLP_ERR_CUDA:
+            lib = load()
+            code, drv, site = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+            lib.linear_logp_last_failure(ctypes.byref(code), ctypes.byref(drv), ctypes.byref(site))
+            detail = [f"check at api.cu:{site.value}"]
+            if code.value:
+                detail.append(f"{lib.linear_logp_cuda_error_name(code.value).decode()} ({code.value})")
+            if drv.value:
+                detail.append(f"tensor-map encoding returned CUresult {drv.value}")
+            msg += " [" + "; ".join(detail) + "]"
+        raise LinearLogpError(fn, status, msg)
 
 
 def profile_start(capacity: int) -> None:

@@ -13,6 +13,25 @@
 #include "llp_internal.h"
 #include "sm103_ptx.cuh"
 
+// Code of the last failed CUDA call made by this library on the calling thread,
+// the last failed driver call's result, and the source line of the check that
+// turned a failure into LLP_ERR_CUDA.
+thread_local int g_last_cuda_error = 0;
+thread_local int g_last_driver_result = 0;
+thread_local int g_last_failure_line = 0;
+
+int fail_cuda(int line) {
+  g_last_failure_line = line;
+  return LLP_ERR_CUDA;
+}
+
+namespace llp {
+cudaError_t note_cuda(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = static_cast<int>(e);
+  return e;
+}
+}  // namespace llp
+
 namespace {
 
 // Kernel status word: a kernel that gives up on a bounded wait records why here.
@@ -31,6 +50,26 @@ struct DeviceInit {
 std::mutex g_mu;
 DeviceInit g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+
+// Tensor-map encoding is a driver call and needs a current context on the
+// calling thread.  A thread whose only CUDA work so far went through an
+// allocator's cache (an autograd worker, say) may have none yet: bind the
+// current device's primary context then (cudaSetDevice does, since CUDA 12),
+// and leave a context the caller made current alone.
+int ensure_context(int dev) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current != nullptr && g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr) return LLP_OK;
+  return llp::note_cuda(cudaSetDevice(dev)) == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
+}
 
 int load_encode_fn() {
   static std::once_flag once;
@@ -40,7 +79,7 @@ int load_encode_fn() {
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
     const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
-      st = LLP_ERR_CUDA;
+      st = fail_cuda(__LINE__);
     } else {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
@@ -51,9 +90,14 @@ int load_encode_fn() {
 // Per-device one-time set-up with that device current: architecture check,
 // shared-memory opt-in for every kernel, SM count, status-word address.
 int init_device(DeviceInit** out) {
+  // A pending, non-sticky error left on this thread by an earlier, unrelated
+  // CUDA call would otherwise be read back after our first launch and taken
+  // for this call's failure; a sticky (context) error persists and is reported.
+  (void)cudaGetLastError();
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::note_cuda(cudaGetDevice(&dev)) != cudaSuccess) return fail_cuda(__LINE__);
   if (dev < 0 || dev >= kMaxDevices) return LLP_ERR_UNSUPPORTED_DEVICE;
+  if (ensure_context(dev) != LLP_OK) return LLP_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceInit& d = g_dev[dev];
   if (!d.done) {
@@ -61,13 +105,13 @@ int init_device(DeviceInit** out) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     }
     if (major != 10 || minor != 3) {
       d.status = LLP_ERR_UNSUPPORTED_DEVICE;
     } else if (llp::fwd_setup(&d.caps) != cudaSuccess || llp::bwd_setup(&d.caps) != cudaSuccess ||
                cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_ptr), g_status_word) != cudaSuccess) {
-      d.status = LLP_ERR_CUDA;
+      d.status = fail_cuda(__LINE__);
     } else {
       d.status = LLP_OK;
     }
@@ -172,7 +216,8 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
                               const_cast<void*>(base), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
+  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
+  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
 }
 
 // Output map of fp32 segment partials [nseg][rows][cols], box {32, 32, 1}:
@@ -185,7 +230,8 @@ int make_map_part(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? LLP_OK : LLP_ERR_CUDA;
+  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
+  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
 }
 
 // Output map of a gradient [rows][D] (bf16) or of its segment partials.
@@ -248,8 +294,8 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
              float* sh_se = nullptr, float* sh_tl = nullptr, bool f16 = false) {
   const FwdLayout L = fwd_layout(N, V);
   CUtensorMap tm_h, tm_w;
-  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return fail_cuda(__LINE__);
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
@@ -271,12 +317,12 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.f16 = f16 ? 1 : 0;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   rec_mark(s, -1);
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return fail_cuda(__LINE__);
   rec_mark(s, kKFwdPartials);
   if (sh_max != nullptr) {
-    if (llp::launch_shard_stats(p, sh_max, sh_se, sh_tl, s) != cudaSuccess) return LLP_ERR_CUDA;
+    if (llp::launch_shard_stats(p, sh_max, sh_se, sh_tl, s) != cudaSuccess) return fail_cuda(__LINE__);
   } else {
-    if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+    if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return fail_cuda(__LINE__);
   }
   rec_mark(s, kKFwdMerge);
   return LLP_OK;
@@ -320,8 +366,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   // B1: dlogits (+ grad_bias partials)
   {
     CUtensorMap tm_h, tm_w;
-    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
+    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return fail_cuda(__LINE__);
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -346,16 +392,16 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
     CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
-    if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32, f16) != LLP_OK) return LLP_ERR_CUDA;
-    if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
+    if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32, f16) != LLP_OK) return fail_cuda(__LINE__);
+    if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s) != cudaSuccess) return fail_cuda(__LINE__);
     rec_mark(s, kKDlogits);
   }
 
   // B2: grad_hidden = dz . W over fixed vocab segments
   if (want_gh) {
     CUtensorMap tm_dz, tm_w_mn;
-    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
+    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
     llp::GradGemmParams p;
     p.rows = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -373,15 +419,15 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
-    if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map_grad_out(&tm_out, p) != LLP_OK) return fail_cuda(__LINE__);
     if (llp::launch_grad_hidden(tm_dz, tm_w_mn, tm_out, p, units, dev->caps, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     rec_mark(s, kKGradHidden);
     if (p.nseg > 1) {
       const cudaError_t e =
           p.f32_out ? llp::launch_segment_sum_f32(p.part, p.nseg, static_cast<long long>(N) * D, grad_hidden_f32, s)
                     : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s, p.f16);
-      if (e != cudaSuccess) return LLP_ERR_CUDA;
+      if (e != cudaSuccess) return fail_cuda(__LINE__);
       rec_mark(s, kKSegSumHidden);
     }
   }
@@ -389,8 +435,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   // B3: grad_weight = dz^T . h over fixed token segments
   if (grad_weight != nullptr) {
     CUtensorMap tm_dz_mn, tm_h_mn;
-    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) return LLP_ERR_CUDA;
-    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
+    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
     llp::GradGemmParams p;
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
@@ -407,13 +453,13 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
-    if (make_map_grad_out(&tm_out, p) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map_grad_out(&tm_out, p) != LLP_OK) return fail_cuda(__LINE__);
     if (llp::launch_grad_weight(tm_dz_mn, tm_h_mn, tm_out, p, units, dev->caps, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     rec_mark(s, kKGradWeight);
     if (p.nseg > 1) {
       if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s, p.f16) != cudaSuccess)
-        return LLP_ERR_CUDA;
+        return fail_cuda(__LINE__);
       rec_mark(s, kKSegSumWeight);
     }
   }
@@ -423,7 +469,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     const int nblocks = static_cast<int>(cdiv(N, llp::kUnitM) * (llp::kUnitM / 32));
     if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
                              s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     rec_mark(s, kKBiasSum);
   }
   return LLP_OK;
@@ -518,9 +564,9 @@ static int bwd_entry(const float* grad_logp, const float* saved_lse, const void*
     // The per-token pointers (hidden, targets, grad_logp, saved_lse) may be NULL.
     if ((st = init_device(&dev)) != LLP_OK) return st;
     if (grad_weight && cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * D * 2, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     if (grad_bias && cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(V) * sizeof(float), s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     return LLP_OK;
   }
   st = check_inputs(hidden, weight, bias, targets, temperature, N, D, V);
@@ -616,21 +662,20 @@ static int fwd_indexed_entry(const void* hidden, const void* weight, const float
   llp::RowSelection sel;
   if (llp::build_row_selection(reinterpret_cast<const long long*>(indices), K, static_cast<int>(N), ws + L.sel, &sel,
                                s) != cudaSuccess)
-    return LLP_ERR_CUDA;
+    return fail_cuda(__LINE__);
   auto* c_hidden = reinterpret_cast<__nv_bfloat16*>(ws + L.c_hidden);
   auto* c_targets = reinterpret_cast<long long*>(ws + L.c_targets);
   float* c_temp = temperature ? reinterpret_cast<float*>(ws + L.c_temp) : nullptr;
   if (llp::gather_selected_rows(sel, static_cast<int>(D), static_cast<const __nv_bfloat16*>(hidden),
                                 reinterpret_cast<const long long*>(targets), temperature, nullptr, nullptr,
                                 ignore_index, c_hidden, c_targets, c_temp, nullptr, nullptr, s) != cudaSuccess)
-    return LLP_ERR_CUDA;
+    return fail_cuda(__LINE__);
   float* c_logp = reinterpret_cast<float*>(ws + L.c_a);
   float* c_lse = reinterpret_cast<float*>(ws + L.c_b);
   st = fwd_core(dev, c_hidden, weight, bias, reinterpret_cast<const int64_t*>(c_targets), c_temp, L.Kc, D, V,
                 ignore_index, c_logp, c_lse, ws + L.inner, s, 0, nullptr, nullptr, nullptr, f16);
   if (st != LLP_OK) return st;
-  return llp::scatter_selected_outputs(sel, c_logp, c_lse, out_logp, out_lse, s) == cudaSuccess ? LLP_OK
-                                                                                                : LLP_ERR_CUDA;
+  return llp::scatter_selected_outputs(sel, c_logp, c_lse, out_logp, out_lse, s) == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
 }
 
 int linear_logp_fwd_indexed(const void* hidden, const void* weight, const float* bias, const int64_t* targets,
@@ -667,11 +712,11 @@ static int bwd_indexed_entry(const float* grad_logp, const float* saved_lse, con
   if (N == 0 || K == 0) {  // nothing selected: every gradient is zero
     if ((st = init_device(&dev)) != LLP_OK) return st;
     if (grad_hidden && N > 0 && cudaMemsetAsync(grad_hidden, 0, static_cast<size_t>(N) * D * 2, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     if (grad_weight && cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * D * 2, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     if (grad_bias && cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(V) * 4, s) != cudaSuccess)
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     return LLP_OK;
   }
   if (indices == nullptr) return LLP_ERR_NULL_POINTER;
@@ -688,7 +733,7 @@ static int bwd_indexed_entry(const float* grad_logp, const float* saved_lse, con
   llp::RowSelection sel;
   if (llp::build_row_selection(reinterpret_cast<const long long*>(indices), K, static_cast<int>(N), ws + L.sel, &sel,
                                s) != cudaSuccess)
-    return LLP_ERR_CUDA;
+    return fail_cuda(__LINE__);
   auto* c_hidden = reinterpret_cast<__nv_bfloat16*>(ws + L.c_hidden);
   auto* c_targets = reinterpret_cast<long long*>(ws + L.c_targets);
   float* c_temp = temperature ? reinterpret_cast<float*>(ws + L.c_temp) : nullptr;
@@ -697,7 +742,7 @@ static int bwd_indexed_entry(const float* grad_logp, const float* saved_lse, con
   if (llp::gather_selected_rows(sel, static_cast<int>(D), static_cast<const __nv_bfloat16*>(hidden),
                                 reinterpret_cast<const long long*>(targets), temperature, grad_logp, saved_lse,
                                 ignore_index, c_hidden, c_targets, c_temp, c_grad, c_lse, s) != cudaSuccess)
-    return LLP_ERR_CUDA;
+    return fail_cuda(__LINE__);
   auto* c_gh = grad_hidden ? reinterpret_cast<__nv_bfloat16*>(ws + L.c_gh) : nullptr;
   st = bwd_core(dev, c_grad, c_lse, c_hidden, weight, bias, reinterpret_cast<const int64_t*>(c_targets), c_temp,
                 L.Kc, D, V, ignore_index, c_gh, grad_weight, grad_bias, ws + L.inner, s, 0, -1, nullptr, f16);
@@ -705,7 +750,7 @@ static int bwd_indexed_entry(const float* grad_logp, const float* saved_lse, con
   if (grad_hidden &&
       llp::scatter_selected_grad_hidden(sel, static_cast<int>(N), static_cast<int>(D), c_gh,
                                         static_cast<__nv_bfloat16*>(grad_hidden), s) != cudaSuccess)
-    return LLP_ERR_CUDA;
+    return fail_cuda(__LINE__);
   return LLP_OK;
 }
 
@@ -790,8 +835,7 @@ int linear_logp_merge_shards(const float* shard_max, const float* shard_sumexp, 
   return llp::launch_merge_shards(shard_max, shard_sumexp, shard_target_logit, static_cast<int>(R),
                                   static_cast<int>(N), reinterpret_cast<const long long*>(targets), global_V,
                                   ignore_index, out_logp, out_lse, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? LLP_OK
-             : LLP_ERR_CUDA;
+             ? LLP_OK : fail_cuda(__LINE__);
 }
 
 static int bwd_shard_entry(const float* grad_logp, const float* lse, const void* hidden, const void* weight_local,
@@ -813,9 +857,9 @@ static int bwd_shard_entry(const float* grad_logp, const float* lse, const void*
   if (N == 0) {
     if ((st = init_device(&dev)) != LLP_OK) return st;
     if (grad_weight_local && cudaMemsetAsync(grad_weight_local, 0, static_cast<size_t>(V_local) * D * 2, s))
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     if (grad_bias_local && cudaMemsetAsync(grad_bias_local, 0, static_cast<size_t>(V_local) * 4, s))
-      return LLP_ERR_CUDA;
+      return fail_cuda(__LINE__);
     return LLP_OK;
   }
   st = check_inputs(hidden, weight_local, bias_local, targets, temperature, N, D, V_local);
@@ -864,8 +908,7 @@ static int sum_partials_entry(const float* parts, int64_t R, int64_t count, void
   if (st != LLP_OK) return st;
   return llp::launch_segment_sum(parts, static_cast<int>(R), count, static_cast<__nv_bfloat16*>(out_bf16),
                                  static_cast<cudaStream_t>(stream), f16 ? 1 : 0) == cudaSuccess
-             ? LLP_OK
-             : LLP_ERR_CUDA;
+             ? LLP_OK : fail_cuda(__LINE__);
 }
 
 int linear_logp_sum_partials(const float* parts, int64_t R, int64_t count, void* out_bf16, void* stream) {
@@ -917,7 +960,7 @@ int fused_logp_fwd(const void* logits, int dtype, int64_t N, int64_t V, const in
       logits, dtype, static_cast<int>(N), static_cast<int>(V), reinterpret_cast<const long long*>(targets),
       ignore_index, static_cast<float*>(workspace), out_logp, out_row_max, out_log_sum,
       fused_vec_ok(logits, dtype, V), static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? LLP_OK : LLP_ERR_CUDA;
+  return e == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
 }
 
 int fused_logp_bwd(const float* grad_logp, const float* row_max, const float* log_sum, const void* logits, int dtype,
@@ -937,7 +980,7 @@ int fused_logp_bwd(const float* grad_logp, const float* row_max, const float* lo
   const cudaError_t e = llp::launch_logits_bwd(
       logits, dtype, static_cast<int>(N), static_cast<int>(V), reinterpret_cast<const long long*>(targets),
       ignore_index, grad_logp, row_max, log_sum, grad_logits, vec, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? LLP_OK : LLP_ERR_CUDA;
+  return e == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
 }
 
 // One thread waits, with the production wait code, on a barrier that nothing
@@ -959,20 +1002,31 @@ int linear_logp_selftest_wait_timeout(unsigned long long limit_ns, void* stream)
   const int st = init_device(&dev);
   if (st != LLP_OK) return st;
   wait_timeout_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(dev->status_ptr, limit_ns);
-  return cudaGetLastError() == cudaSuccess ? LLP_OK : LLP_ERR_CUDA;
+  return llp::launch_result() == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
 }
+
+int linear_logp_last_cuda_error(void) { return g_last_cuda_error; }
+
+int linear_logp_last_failure(int* cuda_error, int* driver_result, int* site) {
+  if (cuda_error) *cuda_error = g_last_cuda_error;
+  if (driver_result) *driver_result = g_last_driver_result;
+  if (site) *site = g_last_failure_line;
+  return LLP_OK;
+}
+
+const char* linear_logp_cuda_error_name(int code) { return cudaGetErrorName(static_cast<cudaError_t>(code)); }
 
 int linear_logp_device_status(void* stream, unsigned int* device_code) {
   DeviceInit* dev = nullptr;
   const int st = init_device(&dev);
   if (st != LLP_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLP_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return fail_cuda(__LINE__);
   unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return LLP_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return fail_cuda(__LINE__);
   if (device_code != nullptr) *device_code = v;
   if (v != 0) {
     const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return LLP_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return fail_cuda(__LINE__);
     return LLP_ERR_DEVICE_TIMEOUT;
   }
   return LLP_OK;
@@ -993,12 +1047,12 @@ static void* g_noalloc_ptr[kMaxDevices] = {};
 // device current.  Returns LLP_OK and the address, or LLP_ERR_CUDA.
 static int noalloc_scratch(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LLP_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail_cuda(__LINE__);
   if (dev < 0 || dev >= kMaxDevices) return LLP_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return LLP_ERR_CUDA;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return fail_cuda(__LINE__);
     g_noalloc_ptr[dev] = ptr;
   }
   *out = g_noalloc_ptr[dev];
@@ -1026,8 +1080,8 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   CUtensorMap tm_h, tm_w;
-  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return LLP_ERR_CUDA;
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return fail_cuda(__LINE__);
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return fail_cuda(__LINE__);
 
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   llp::FwdParams p;
@@ -1051,8 +1105,8 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   p.f16 = 0;
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return LLP_ERR_CUDA;
-  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return LLP_ERR_CUDA;
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return fail_cuda(__LINE__);
+  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return fail_cuda(__LINE__);
   return LLP_OK;
 }
 
@@ -1062,7 +1116,7 @@ int linear_logp_profile_start(int capacity) {
   const size_t need = static_cast<size_t>(capacity) * 2 + 2;
   while (g_rec.events.size() < need) {
     cudaEvent_t e;
-    if (cudaEventCreate(&e) != cudaSuccess) return LLP_ERR_CUDA;
+    if (cudaEventCreate(&e) != cudaSuccess) return fail_cuda(__LINE__);
     g_rec.events.push_back(e);
   }
   g_rec.ids.assign(g_rec.events.size(), -1);
@@ -1077,13 +1131,13 @@ int linear_logp_profile_stop(int* kernel_ids, float* ms, int capacity) {
   std::lock_guard<std::mutex> lock(g_rec.mu);
   g_rec.on = false;
   if (g_rec.used == 0) return 0;
-  if (cudaEventSynchronize(g_rec.events[g_rec.used - 1]) != cudaSuccess) return LLP_ERR_CUDA;
+  if (cudaEventSynchronize(g_rec.events[g_rec.used - 1]) != cudaSuccess) return fail_cuda(__LINE__);
   int n = 0;
   for (int i = 1; i < g_rec.used; ++i) {
     if (g_rec.ids[i] < 0) continue;
     if (n < capacity && kernel_ids != nullptr && ms != nullptr) {
       float t = 0.f;
-      if (cudaEventElapsedTime(&t, g_rec.events[i - 1], g_rec.events[i]) != cudaSuccess) return LLP_ERR_CUDA;
+      if (cudaEventElapsedTime(&t, g_rec.events[i - 1], g_rec.events[i]) != cudaSuccess) return fail_cuda(__LINE__);
       kernel_ids[n] = g_rec.ids[i];
       ms[n] = t;
     }

@@ -385,7 +385,7 @@ cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __n
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
   segment_sum_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out, f16);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, cudaStream_t s) {
@@ -394,13 +394,13 @@ cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count,
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
   segment_sum_f32_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s) {
   const int threads = 256;
   bias_sum_kernel<<<(V + threads - 1) / threads, threads, 0, s>>>(gb_part, nblocks, V, out);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 }  // namespace llp

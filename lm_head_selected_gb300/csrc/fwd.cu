@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(256) merge_shards_kernel(const float* __restri
 cudaError_t launch_shard_stats(const FwdParams& p, float* out_max, float* out_sumexp, float* out_tlogit,
                                cudaStream_t s) {
   shard_stats_kernel<<<(p.N + kMergeRows - 1) / kMergeRows, 256, 0, s>>>(p, out_max, out_sumexp, out_tlogit);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 cudaError_t launch_merge_shards(const float* mx, const float* se, const float* tl, int R, int N,
@@ -284,7 +284,7 @@ cudaError_t launch_merge_shards(const float* mx, const float* se, const float* t
                                 float* out_lse, cudaStream_t s) {
   merge_shards_kernel<<<(N + 255) / 256, 256, 0, s>>>(mx, se, tl, R, N, targets, global_V, ignore_index, out_logp,
                                                       out_lse);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 cudaError_t fwd_setup(LaunchCaps* caps) {
@@ -308,7 +308,7 @@ cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w
 
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s) {
   fwd_merge_kernel<<<(p.N + kMergeRows - 1) / kMergeRows, 256, 0, s>>>(p, out_logp, out_lse);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 }  // namespace llp

@@ -549,7 +549,7 @@ inline cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Cfg>, a, b, c, p);
+  return note_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Cfg>, a, b, c, p));
 }
 
 // One-time set-up per kernel: shared-memory opt-in and the number of clusters

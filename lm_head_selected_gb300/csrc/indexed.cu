@@ -190,19 +190,19 @@ cudaError_t build_row_selection(const long long* idx, long long K, int N, void* 
   if (e != cudaSuccess) return e;
   if (K > 0) {
     mark_rows_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, s>>>(idx, K, N, sel->mask);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_result()) != cudaSuccess) return e;
   }
   count_rows_kernel<<<nb, kScanBlock, 0, s>>>(sel->mask, N, counts);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_result()) != cudaSuccess) return e;
   scan_counts_kernel<<<1, 1024, 0, s>>>(counts, nb, sel->total);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_result()) != cudaSuccess) return e;
   place_rows_kernel<<<nb, kScanBlock, 0, s>>>(sel->mask, N, counts, sel->rows);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_result()) != cudaSuccess) return e;
   if (K > 0) {
     pad_rows_kernel<<<(sel->K + 255) / 256, 256, 0, s>>>(sel->rows, sel->K, sel->total);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_result()) != cudaSuccess) return e;
     slot_of_kernel<<<(sel->K + 255) / 256, 256, 0, s>>>(sel->rows, sel->K, sel->slot_of);
-    e = cudaGetLastError();
+    e = launch_result();
   }
   return e;
 }
@@ -215,21 +215,21 @@ cudaError_t gather_selected_rows(const RowSelection& sel, int D, const __nv_bflo
   if (sel.K == 0) return cudaSuccess;
   gather_rows_kernel<<<sel.K, 128, 0, s>>>(sel.rows, sel.K, D, hidden, targets, temperature, grad_logp, lse,
                                            ignore_index, c_hidden, c_targets, c_temperature, c_grad, c_lse);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 cudaError_t scatter_selected_outputs(const RowSelection& sel, const float* c_logp, const float* c_lse, float* logp,
                                      float* lse, cudaStream_t s) {
   if (sel.K == 0) return cudaSuccess;
   scatter_outputs_kernel<<<(sel.K + 255) / 256, 256, 0, s>>>(sel.rows, sel.K, c_logp, c_lse, logp, lse);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 cudaError_t scatter_selected_grad_hidden(const RowSelection& sel, int N, int D, const __nv_bfloat16* c_gh,
                                          __nv_bfloat16* gh, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   scatter_grad_hidden_kernel<<<N, 128, 0, s>>>(sel.mask, sel.slot_of, N, D, c_gh, gh);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 }  // namespace llp

@@ -108,6 +108,12 @@ struct GradGemmParams {
   int f16;             // operands and the 16-bit output are IEEE fp16 (else bf16)
 };
 
+// Records a failed CUDA call's code for linear_logp_last_cuda_error (per calling
+// thread) and returns it unchanged.
+cudaError_t note_cuda(cudaError_t e);
+// The error of the launch just made on this thread (cudaGetLastError, recorded).
+inline cudaError_t launch_result() { return note_cuda(cudaGetLastError()); }
+
 // Launchers (return the launch error, never synchronise).  `units` is the
 // number of work units; the grid is min(units, resident groups) groups.
 cudaError_t fwd_setup(LaunchCaps* caps);

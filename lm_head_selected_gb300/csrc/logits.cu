@@ -303,11 +303,11 @@ cudaError_t launch_fwd_dt(const void* z, int N, int V, const long long* targets,
   else
     logits_split_kernel<DT, false><<<static_cast<unsigned>(items), kLThreads, 0, s>>>(static_cast<const T*>(z), N, V,
                                                                                      S, pm, ps);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_result();
   if (e != cudaSuccess) return e;
   logits_merge_kernel<DT><<<(N + 255) / 256, 256, 0, s>>>(static_cast<const T*>(z), N, V, S, targets, ignore_index, pm,
                                                           ps, logp, row_max, log_sum);
-  return cudaGetLastError();
+  return launch_result();
 }
 
 template <int DT>
@@ -323,7 +323,7 @@ cudaError_t launch_bwd_dt(const void* z, int N, int V, const long long* targets,
   else
     logits_grad_kernel<DT, false><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(
         static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, static_cast<T*>(grad));
-  return cudaGetLastError();
+  return launch_result();
 }
 
 }  // namespace

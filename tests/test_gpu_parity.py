@@ -166,3 +166,40 @@ def test_bias_at_unaligned_offset():
     gh, gw, gb = gpu_bwd(d, lse)
     check_device_status()
     check_backward(inp, gh, gw, gb)
+
+
+def test_call_from_a_fresh_thread():
+    """A thread whose first CUDA work is this library's call (no context bound on
+    it yet; an autograd worker whose tensors come from the allocator's cache is one)
+    gets the same results as the main thread."""
+    import threading
+
+    import lm_head_selected_gb300 as llp
+    inp = workloads.make_inputs(64, 256, 4096, seed=3, weight_std=0.125, bias_std=0.1, n_ignore=4, grad_std=1.0)
+    d = to_device(inp)
+    logp0, lse0 = gpu_fwd(d)
+    gh0, gw0, gb0 = gpu_bwd(d, lse0)
+    logp = torch.empty_like(logp0)
+    lse = torch.empty_like(lse0)
+    ws_f = torch.empty(llp.fwd_workspace_bytes(inp.N, inp.D, inp.V), dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty(llp.bwd_workspace_bytes(inp.N, inp.D, inp.V, True), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    out, err = {}, []
+
+    def work():
+        try:
+            llp.linear_logp_fwd(d["hidden"], d["weight"], d["targets"], d["bias"], None, workspace=ws_f, out=(logp, lse))
+            out["g"] = llp.linear_logp_bwd(d["grad_logp"], lse, d["hidden"], d["weight"], d["targets"], d["bias"],
+                                           workspace=ws_b)
+            torch.cuda.synchronize()
+        except Exception as e:  # reported in the main thread
+            err.append(e)
+
+    th = threading.Thread(target=work)
+    th.start()
+    th.join()
+    assert not err, err
+    check_device_status()
+    gh, gw, gb = out["g"]
+    assert torch.equal(logp, logp0) and torch.equal(lse, lse0)
+    assert torch.equal(gh, gh0) and torch.equal(gw, gw0) and torch.equal(gb, gb0)
