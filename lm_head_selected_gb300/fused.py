@@ -12,6 +12,7 @@ from typing import Optional
 import torch
 
 from . import _lib
+from .ops import on_tensor_device
 
 IGNORE_INDEX = -100
 _DTYPES = {torch.bfloat16: 0, torch.float32: 1}
@@ -34,6 +35,7 @@ def _check(logits: torch.Tensor, targets: torch.Tensor):
         raise ValueError("targets must be contiguous")
 
 
+@on_tensor_device
 def fused_logp_fwd(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = IGNORE_INDEX,
                    workspace: Optional[torch.Tensor] = None):
     """(logp, row_max, log_sum), each fp32 [N]; lse = row_max + log_sum."""
@@ -54,6 +56,7 @@ def fused_logp_fwd(logits: torch.Tensor, targets: torch.Tensor, ignore_index: in
     return logp, row_max, log_sum
 
 
+@on_tensor_device
 def fused_logp_bwd(grad_logp: torch.Tensor, row_max: torch.Tensor, log_sum: torch.Tensor, logits: torch.Tensor,
                    targets: torch.Tensor, ignore_index: int = IGNORE_INDEX,
                    out: Optional[torch.Tensor] = None) -> torch.Tensor:

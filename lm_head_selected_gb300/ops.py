@@ -17,6 +17,8 @@ Entry points mirror the C ABI names:
 from __future__ import annotations
 
 import ctypes
+import functools
+import itertools
 from typing import Optional, Tuple
 
 import torch
@@ -24,6 +26,19 @@ import torch
 from . import _lib
 
 IGNORE_INDEX = -100
+
+
+def on_tensor_device(fn):
+    """Run a wrapper with its first CUDA tensor argument's device current: the C
+    ABI launches on the current device, which need not be the tensors' one."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        for a in itertools.chain(args, kwargs.values()):
+            if isinstance(a, torch.Tensor) and a.is_cuda:
+                with torch.cuda.device(a.device):
+                    return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return wrapper
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -88,6 +103,7 @@ def _workspace(nbytes: int, device, given: Optional[torch.Tensor]):
     return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
 
 
+@on_tensor_device
 def linear_logp_fwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                     bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
                     ignore_index: int = IGNORE_INDEX, workspace: Optional[torch.Tensor] = None,
@@ -110,6 +126,7 @@ def linear_logp_fwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.T
     return logp, lse
 
 
+@on_tensor_device
 def linear_logp_fwd_noalloc(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                             bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
                             ignore_index: int = IGNORE_INDEX,
@@ -131,6 +148,7 @@ def linear_logp_fwd_noalloc(hidden: torch.Tensor, weight: torch.Tensor, targets:
     return logp, lse
 
 
+@on_tensor_device
 def linear_logp_bwd(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hidden: torch.Tensor,
                     weight: torch.Tensor, targets: torch.Tensor, bias: Optional[torch.Tensor] = None,
                     temperature: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,
@@ -163,6 +181,7 @@ def _check_indices(indices: torch.Tensor, device) -> torch.Tensor:
     return indices.reshape(-1).contiguous()
 
 
+@on_tensor_device
 def linear_logp_fwd_indexed(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                             indices: torch.Tensor, bias: Optional[torch.Tensor] = None,
                             temperature: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,
@@ -189,6 +208,7 @@ def linear_logp_fwd_indexed(hidden: torch.Tensor, weight: torch.Tensor, targets:
     return logp, lse
 
 
+@on_tensor_device
 def linear_logp_bwd_indexed(grad_logp: torch.Tensor, saved_lse: torch.Tensor, hidden: torch.Tensor,
                             weight: torch.Tensor, targets: torch.Tensor, indices: torch.Tensor,
                             bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
@@ -218,7 +238,8 @@ def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the kernel status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     code = ctypes.c_uint(0)
-    st = _lib.load().linear_logp_device_status(_stream(dev), ctypes.byref(code))
+    with torch.cuda.device(dev):
+        st = _lib.load().linear_logp_device_status(_stream(dev), ctypes.byref(code))
     if st not in (_lib.LLP_OK, _lib.LLP_ERR_DEVICE_TIMEOUT):
         _lib.check("linear_logp_device_status", st)
     return int(code.value)

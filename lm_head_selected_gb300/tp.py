@@ -26,9 +26,10 @@ import torch
 import torch.distributed as dist
 
 from . import _lib
-from .ops import IGNORE_INDEX, _check_inputs, _need, _ptr, _stream, _workspace
+from .ops import IGNORE_INDEX, _check_inputs, _need, _ptr, _stream, _workspace, on_tensor_device
 
 
+@on_tensor_device
 def fwd_shard(hidden, weight_local, targets, vocab_start, bias_local=None, temperature=None,
               ignore_index=IGNORE_INDEX):
     """-> stats fp32 [3, N]: (max, sum of exp(z - max), target logit or -inf) of this shard.
@@ -45,6 +46,7 @@ def fwd_shard(hidden, weight_local, targets, vocab_start, bias_local=None, tempe
     return stats
 
 
+@on_tensor_device
 def merge_shards(gathered, targets, global_vocab_size, ignore_index=IGNORE_INDEX):
     """gathered fp32 [R, 3, N] in rank order -> (logp, lse)."""
     R, three, N = gathered.shape
@@ -60,6 +62,7 @@ def merge_shards(gathered, targets, global_vocab_size, ignore_index=IGNORE_INDEX
     return logp, lse
 
 
+@on_tensor_device
 def bwd_shard(grad_logp, lse, hidden, weight_local, targets, vocab_start, global_vocab_size, bias_local=None,
               temperature=None, ignore_index=IGNORE_INDEX, need_weight=True, need_bias=True):
     """-> (grad_hidden contribution fp32 [N, D], local grad_weight in the inputs' dtype, local grad_bias fp32)."""
@@ -79,6 +82,7 @@ def bwd_shard(grad_logp, lse, hidden, weight_local, targets, vocab_start, global
     return gh, gw, gb
 
 
+@on_tensor_device
 def sum_partials(parts, dtype=torch.bfloat16):
     """parts fp32 [R, ...] -> sum over R in ascending order, rounded once to dtype (bf16 or fp16)."""
     if dtype not in (torch.bfloat16, torch.float16):
