@@ -34,8 +34,9 @@
  *     memory, row-major and contiguous.  bf16 tensors are passed as raw
  *     16-bit storage (void*).  The caller owns every buffer; the library
  *     allocates nothing and keeps no per-call state.
- *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
- *     enqueued on it; the library never synchronises.
+ *   - `stream` is a cudaStream_t of the current device (NULL = legacy default
+ *     stream).  Work is enqueued on it; the library never synchronises.  A
+ *     thread with no current context gets the current device's primary one.
  *   - Alignment: hidden, weight, grad_hidden, grad_weight and workspace must be
  *     16-byte aligned; bias and other float arrays 4-byte aligned;
  *     targets 8-byte aligned.
