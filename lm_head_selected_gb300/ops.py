@@ -264,13 +264,20 @@ class _LinearLogp(torch.autograd.Function):
 
 def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                 bias: Optional[torch.Tensor] = None, temperature: Optional[torch.Tensor] = None,
-                ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
+                ignore_index: int = IGNORE_INDEX, *, tp_group=None, vocab_start_index: int = 0,
+                global_vocab_size: Optional[int] = None) -> torch.Tensor:
     """log_softmax((hidden @ weight^T + bias) / temperature)[targets], fp32, with autograd.
 
     hidden [..., D] and weight [V, D] both bf16 or both fp16, targets [...] int64,
     bias [V] fp32, temperature [...] fp32 (per token).  Returns fp32 with the
     leading shape of targets.  Gradients reach hidden and weight in their dtype
     and bias as fp32.
+
+    The "Fused Linear LogP" entry point's vocab-parallel arguments: with a
+    ``tp_group``, ``weight`` / ``bias`` are this rank's rows ``vocab_start_index
+    .. + V_local - 1`` of a head of ``global_vocab_size`` rows (default: the sum
+    of the ranks' V_local), targets are global ids, and the shards' statistics
+    are merged in ascending rank order (see ``tp.linear_logp_vocab_parallel``).
     """
     lead = targets.shape
     D = hidden.shape[-1]
@@ -279,6 +286,19 @@ def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tenso
     tau = None if temperature is None else temperature.reshape(-1)
     if h2.shape[0] != t1.shape[0]:
         raise ValueError("hidden and targets must share the leading shape")
-    out = _LinearLogp.apply(h2.contiguous(), weight, bias, t1.contiguous(),
-                            None if tau is None else tau.contiguous(), int(ignore_index))
+    tau = None if tau is None else tau.contiguous()
+    if tp_group is not None:
+        from . import tp
+        if global_vocab_size is None:
+            import torch.distributed as dist
+            n = torch.tensor([weight.shape[0]], dtype=torch.int64, device=weight.device)
+            dist.all_reduce(n, group=tp_group)
+            global_vocab_size = int(n.item())
+        out = tp.linear_logp_vocab_parallel(h2.contiguous(), weight, t1.contiguous(), bias, tau, group=tp_group,
+                                            vocab_start=vocab_start_index, global_vocab_size=global_vocab_size,
+                                            ignore_index=ignore_index)
+        return out.reshape(lead)
+    if vocab_start_index != 0 or global_vocab_size not in (None, weight.shape[0]):
+        raise ValueError("vocab_start_index / global_vocab_size describe a vocab shard: pass tp_group too")
+    out = _LinearLogp.apply(h2.contiguous(), weight, bias, t1.contiguous(), tau, int(ignore_index))
     return out.reshape(lead)

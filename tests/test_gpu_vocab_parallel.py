@@ -93,3 +93,39 @@ def test_nemotron_head_two_shards():
     gh_ref, _, _ = oracle.backward(np64(inp.grad_logp), *a, rows=rows, need_weight=False)
     # grad_hidden of a row depends only on that row: compare on the sampled rows
     assert_close("grad_hidden[rows]", np64(gh)[rows], gh_ref[rows], GH_ATOL, GH_RTOL)
+
+
+def test_entry_point_tp_group_of_one_matches_plain():
+    """``linear_logp(..., tp_group=...)`` (the pages' entry point) over a group of
+    one rank gives the plain path's logp and gradients bitwise: with one shard the
+    merges reduce to the same expressions and roundings."""
+    import os
+    import socket
+
+    import torch.distributed as dist
+
+    import lm_head_selected_gb300 as llp
+    if dist.is_initialized():
+        pytest.skip("a process group already exists")
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        inp = workloads.make_inputs(96, 256, 3000, seed=77, weight_std=0.12, bias_std=0.2, n_ignore=3,
+                                    grad_std=1.0)
+        d = to_device(inp)
+        res = []
+        for kw in ({}, {"tp_group": dist.group.WORLD}):
+            h = d["hidden"].view(2, 48, 256).clone().requires_grad_(True)
+            w = d["weight"].clone().requires_grad_(True)
+            b = d["bias"].clone().requires_grad_(True)
+            out = llp.linear_logp(h, w, d["targets"].view(2, 48), b, **kw)
+            (out * d["grad_logp"].view(2, 48)).sum().backward()
+            res.append((out.detach(), h.grad, w.grad, b.grad))
+        check_device_status()
+        for a, c in zip(*res):
+            assert torch.equal(a, c)
+    finally:
+        dist.destroy_process_group()
