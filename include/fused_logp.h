@@ -23,8 +23,8 @@
  *
  * Conventions as in linear_logp.h: device pointers, caller-owned buffers, work
  * enqueued on `stream`, arguments checked before anything is enqueued, the same
- * LLP_* status codes.  z is contiguous row-major [N, V] in bf16 (dtype 0) or
- * fp32 (dtype 1); grad_z has the same dtype.  Per-row results do not depend on
+ * LLP_* status codes.  z is contiguous row-major [N, V] in bf16 (dtype 0),
+ * fp32 (dtype 1) or fp16 (dtype 2); grad_z has the same dtype.  Per-row results do not depend on
  * N and are identical across runs.  16-byte aligned rows (z base and V * element
  * size multiples of 16) take the vectorised path; other layouts still work.
  */
@@ -40,6 +40,7 @@ extern "C" {
 
 #define FUSED_LOGP_DTYPE_BF16 0
 #define FUSED_LOGP_DTYPE_F32 1
+#define FUSED_LOGP_DTYPE_F16 2
 
 /* Workspace bytes fused_logp_fwd needs (per-row, per-vocab-split max / sum pairs). */
 size_t fused_logp_workspace_bytes(int64_t N, int64_t V);

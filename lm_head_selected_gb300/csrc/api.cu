@@ -923,18 +923,19 @@ int linear_logp_sum_partials_f16(const float* parts, int64_t R, int64_t count, v
 // Logits-input fused log-prob (include/fused_logp.h).
 // ----------------------------------------------------------------------------
 static int fused_check(const void* logits, int dtype, int64_t N, int64_t V, const int64_t* targets) {
-  if (dtype != FUSED_LOGP_DTYPE_BF16 && dtype != FUSED_LOGP_DTYPE_F32) return LLP_ERR_BAD_SHAPE;
+  if (dtype != FUSED_LOGP_DTYPE_BF16 && dtype != FUSED_LOGP_DTYPE_F32 && dtype != FUSED_LOGP_DTYPE_F16)
+    return LLP_ERR_BAD_SHAPE;
   if (N < 0 || V < 1 || N > kLim31 || V > kLim31 || !product_ok(N, V)) return LLP_ERR_BAD_SHAPE;
   if (N * cdiv(V, llp::kLogitsSplit) > kLim31) return LLP_ERR_BAD_SHAPE;
   if (N == 0) return LLP_OK;
   if (logits == nullptr || targets == nullptr) return LLP_ERR_NULL_POINTER;
-  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_BF16 ? 2 : 4;
+  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_F32 ? 4 : 2;
   if (!aligned(logits, es) || !aligned(targets, 8)) return LLP_ERR_MISALIGNED;
   return LLP_OK;
 }
 
 static bool fused_vec_ok(const void* p, int dtype, int64_t V) {
-  const int64_t es = dtype == FUSED_LOGP_DTYPE_BF16 ? 2 : 4;
+  const int64_t es = dtype == FUSED_LOGP_DTYPE_F32 ? 4 : 2;
   return aligned(p, 16) && ((V * es) % 16) == 0;
 }
 
@@ -971,7 +972,7 @@ int fused_logp_bwd(const float* grad_logp, const float* row_max, const float* lo
   if (N == 0) return LLP_OK;
   if (grad_logp == nullptr || row_max == nullptr || log_sum == nullptr || grad_logits == nullptr)
     return LLP_ERR_NULL_POINTER;
-  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_BF16 ? 2 : 4;
+  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_F32 ? 4 : 2;
   if (!aligned(grad_logp, 4) || !aligned(row_max, 4) || !aligned(log_sum, 4) || !aligned(grad_logits, es))
     return LLP_ERR_MISALIGNED;
   DeviceInit* dev = nullptr;

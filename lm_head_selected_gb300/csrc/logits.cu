@@ -15,6 +15,7 @@
 // writes every gradient once).  The split width and the reduction trees depend
 // on V only, so a row's results are the same for every N and every run.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "llp_internal.h"
 #include "sm103_ptx.cuh"
@@ -117,6 +118,49 @@ struct Vec<kDtypeF32> {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
   static __device__ __forceinline__ void store1(T* p, float v) { *p = v; }
+};
+
+template <>
+struct Vec<kDtypeF16> {
+  static constexpr int W = 8;
+  using T = __half;
+  static __device__ __forceinline__ float load1(const T* p) { return __half2float(*p); }
+  // As the bf16 form; fp16 -inf is 0xFC00.
+  static __device__ __forceinline__ uint4 load_raw(const T* p, int n_valid, bool vec) {
+    if (vec && n_valid >= W) return __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t w[4];
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (2 * i < n_valid) ? q[2 * i] : 0xFC00u;
+      const uint32_t hi = (2 * i + 1 < n_valid) ? q[2 * i + 1] : 0xFC00u;
+      w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  static __device__ __forceinline__ void unpack(const uint4& r, float (&v)[W]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void load(const T* p, float (&v)[W]) {
+    unpack(__ldg(reinterpret_cast<const uint4*>(p)), v);
+  }
+  static __device__ __forceinline__ void store(T* p, const float (&v)[W]) {
+    uint4 r;
+    __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]), c = __floats2half2_rn(v[4], v[5]),
+            d = __floats2half2_rn(v[6], v[7]);
+    r.x = *reinterpret_cast<uint32_t*>(&a);
+    r.y = *reinterpret_cast<uint32_t*>(&b);
+    r.z = *reinterpret_cast<uint32_t*>(&c);
+    r.w = *reinterpret_cast<uint32_t*>(&d);
+    *reinterpret_cast<uint4*>(p) = r;
+  }
+  static __device__ __forceinline__ void store1(T* p, float v) { *p = __float2half_rn(v); }
 };
 
 // Merge (m, s) pairs: s is a sum of exp(x - m).
@@ -331,6 +375,8 @@ cudaError_t launch_bwd_dt(const void* z, int N, int V, const long long* targets,
 cudaError_t launch_logits_fwd(const void* z, int dtype, int N, int V, const long long* targets,
                               long long ignore_index, float* part, float* logp, float* row_max, float* log_sum,
                               bool vec, cudaStream_t s) {
+  if (dtype == kDtypeF16)
+    return launch_fwd_dt<kDtypeF16>(z, N, V, targets, ignore_index, part, logp, row_max, log_sum, vec, s);
   return dtype == kDtypeBF16 ? launch_fwd_dt<kDtypeBF16>(z, N, V, targets, ignore_index, part, logp, row_max,
                                                          log_sum, vec, s)
                              : launch_fwd_dt<kDtypeF32>(z, N, V, targets, ignore_index, part, logp, row_max, log_sum,
@@ -340,6 +386,8 @@ cudaError_t launch_logits_fwd(const void* z, int dtype, int N, int V, const long
 cudaError_t launch_logits_bwd(const void* z, int dtype, int N, int V, const long long* targets,
                               long long ignore_index, const float* grad_logp, const float* row_max,
                               const float* log_sum, void* grad, bool vec, cudaStream_t s) {
+  if (dtype == kDtypeF16)
+    return launch_bwd_dt<kDtypeF16>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum, grad, vec, s);
   return dtype == kDtypeBF16 ? launch_bwd_dt<kDtypeBF16>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum,
                                                          grad, vec, s)
                              : launch_bwd_dt<kDtypeF32>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum,

@@ -1,7 +1,7 @@
 """PyTorch-facing wrappers of the logits-input fused log-prob (include/fused_logp.h).
 
 Argument marshalling only; the computation runs in ``liblinear_logp.so``.
-logits [N, V] (or [..., V]) bf16 or fp32, contiguous, on a CUDA device;
+logits [N, V] (or [..., V]) bf16, fp16 or fp32, contiguous, on a CUDA device;
 targets int64 with the logits' leading shape.
 """
 from __future__ import annotations
@@ -15,7 +15,7 @@ from . import _lib
 from .ops import on_tensor_device
 
 IGNORE_INDEX = -100
-_DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+_DTYPES = {torch.bfloat16: 0, torch.float32: 1, torch.float16: 2}
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -26,7 +26,7 @@ def _check(logits: torch.Tensor, targets: torch.Tensor):
     if not isinstance(logits, torch.Tensor) or logits.device.type != "cuda":
         raise ValueError("logits must be a CUDA tensor; this op has no CPU path")
     if logits.dtype not in _DTYPES:
-        raise TypeError(f"logits must be bf16 or fp32, got {logits.dtype}")
+        raise TypeError(f"logits must be bf16, fp16 or fp32, got {logits.dtype}")
     if logits.dim() != 2 or not logits.is_contiguous():
         raise ValueError("logits must be a contiguous [N, V] tensor")
     if targets.dtype != torch.int64 or targets.device != logits.device or targets.shape != (logits.shape[0],):

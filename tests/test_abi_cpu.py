@@ -137,7 +137,7 @@ def test_fused_rejects_bad_arguments_on_host(lib):
         f(k.get("z", 0x1000)), k.get("dt", 0), k.get("N", 4), k.get("V", 100), f(k.get("t", 0x2000)), -100,
         f(k.get("lp", 0x3000)), f(k.get("m", 0x4000)), f(k.get("ls", 0x5000)), f(k.get("ws", 0x6000)),
         k.get("wsb", 1 << 20), None)
-    assert fwd(dt=2) == _lib.LLP_ERR_BAD_SHAPE
+    assert fwd(dt=3) == _lib.LLP_ERR_BAD_SHAPE  # dtypes: 0 bf16, 1 fp32, 2 fp16
     assert fwd(V=0) == _lib.LLP_ERR_BAD_SHAPE
     assert fwd(z=0) == _lib.LLP_ERR_NULL_POINTER
     assert fwd(t=0) == _lib.LLP_ERR_NULL_POINTER

@@ -13,7 +13,8 @@ from oracle import logits_logp as lo
 pytestmark = pytest.mark.gpu
 
 LOGP_ATOL = 5e-3
-TOL = {torch.float32: (1e-5, 1e-4), torch.bfloat16: (1e-3, 1e-2)}  # grad atol, rtol (bf16: one output rounding)
+# grad atol, rtol (16-bit types: one output rounding)
+TOL = {torch.float32: (1e-5, 1e-4), torch.bfloat16: (1e-3, 1e-2), torch.float16: (1e-4, 2e-3)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -64,7 +65,7 @@ def _check(z, t, gl):
     return logp, m, ls, grad
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.float16])
 @pytest.mark.parametrize("N,V", [(64, 4096), (37, 50257), (5, 131072), (300, 16385), (1, 1), (130, 32768)])
 def test_parity(dtype, N, V):
     z, t, gl = _problem(N, V, dtype, seed=N + V, shift_row=0 if dtype == torch.float32 else None)
