@@ -56,6 +56,30 @@ int fused_logp_bwd(const float* grad_logp, const float* row_max, const float* lo
                    int64_t N, int64_t V, const int64_t* targets, int64_t ignore_index, void* grad_logits,
                    void* stream);
 
+/*
+ * Row-subset (indexed) forms ("recursive deterministic LogP autograd on B200",
+ * Indexed semantics: full output row shape, duplicate indices idempotent,
+ * out-of-range indices ignored, zero derivatives for rows not selected).
+ * `indices` [K] int64 (device) names the rows.
+ *   fused_logp_fwd_indexed writes out_logp / out_row_max / out_log_sum for each
+ *     selected row (bitwise what fused_logp_fwd gives that row) and leaves the
+ *     other entries untouched.  Workspace: fused_logp_fwd_indexed_workspace_bytes.
+ *   fused_logp_bwd_indexed writes the full grad_logits [N, V]: selected rows as
+ *     fused_logp_bwd computes them, every other row zero.  row_max / log_sum /
+ *     grad_logp are read on selected rows only.  Workspace:
+ *     fused_logp_bwd_indexed_workspace_bytes (K = 0 selects nothing).
+ */
+size_t fused_logp_fwd_indexed_workspace_bytes(int64_t N, int64_t V, int64_t K);
+size_t fused_logp_bwd_indexed_workspace_bytes(int64_t N, int64_t K);
+int fused_logp_fwd_indexed(const void* logits, int dtype, int64_t N, int64_t V, const int64_t* targets,
+                           int64_t ignore_index, const int64_t* indices, int64_t K, float* out_logp,
+                           float* out_row_max, float* out_log_sum, void* workspace, size_t workspace_bytes,
+                           void* stream);
+int fused_logp_bwd_indexed(const float* grad_logp, const float* row_max, const float* log_sum, const void* logits,
+                           int dtype, int64_t N, int64_t V, const int64_t* targets, int64_t ignore_index,
+                           const int64_t* indices, int64_t K, void* grad_logits, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -56,6 +56,10 @@ EXPORTED_FUSED = (
     "fused_logp_workspace_bytes",
     "fused_logp_fwd",
     "fused_logp_bwd",
+    "fused_logp_fwd_indexed_workspace_bytes",
+    "fused_logp_bwd_indexed_workspace_bytes",
+    "fused_logp_fwd_indexed",
+    "fused_logp_bwd_indexed",
 )
 DEVICE_SELFTEST_CODE = 6
 LLP_ERR_SCRATCH_LIMIT = -8
@@ -160,6 +164,16 @@ def load() -> ctypes.CDLL:
         lib.fused_logp_fwd.restype = ctypes.c_int
         lib.fused_logp_bwd.argtypes = [_p, _p, _p, _p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _p]
         lib.fused_logp_bwd.restype = ctypes.c_int
+        lib.fused_logp_fwd_indexed_workspace_bytes.argtypes = [_i64, _i64, _i64]
+        lib.fused_logp_fwd_indexed_workspace_bytes.restype = _size
+        lib.fused_logp_bwd_indexed_workspace_bytes.argtypes = [_i64, _i64]
+        lib.fused_logp_bwd_indexed_workspace_bytes.restype = _size
+        lib.fused_logp_fwd_indexed.argtypes = [_p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _i64, _p, _p, _p, _p,
+                                               _size, _p]
+        lib.fused_logp_fwd_indexed.restype = ctypes.c_int
+        lib.fused_logp_bwd_indexed.argtypes = [_p, _p, _p, _p, ctypes.c_int, _i64, _i64, _p, _i64, _p, _i64, _p, _p,
+                                               _size, _p]
+        lib.fused_logp_bwd_indexed.restype = ctypes.c_int
         _lib = lib
         return lib
 

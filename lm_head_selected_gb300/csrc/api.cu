@@ -958,7 +958,7 @@ int fused_logp_fwd(const void* logits, int dtype, int64_t N, int64_t V, const in
   DeviceInit* dev = nullptr;
   if ((st = init_device(&dev)) != LLP_OK) return st;
   const cudaError_t e = llp::launch_logits_fwd(
-      logits, dtype, static_cast<int>(N), static_cast<int>(V), reinterpret_cast<const long long*>(targets),
+      logits, dtype, static_cast<int>(N), nullptr, static_cast<int>(V), reinterpret_cast<const long long*>(targets),
       ignore_index, static_cast<float*>(workspace), out_logp, out_row_max, out_log_sum,
       fused_vec_ok(logits, dtype, V), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
@@ -980,7 +980,84 @@ int fused_logp_bwd(const float* grad_logp, const float* row_max, const float* lo
   const bool vec = fused_vec_ok(logits, dtype, V) && fused_vec_ok(grad_logits, dtype, V);
   const cudaError_t e = llp::launch_logits_bwd(
       logits, dtype, static_cast<int>(N), static_cast<int>(V), reinterpret_cast<const long long*>(targets),
-      ignore_index, grad_logp, row_max, log_sum, grad_logits, vec, static_cast<cudaStream_t>(stream));
+      ignore_index, grad_logp, row_max, log_sum, nullptr, grad_logits, vec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
+}
+
+// Row-subset forms: the index list becomes a byte mask and an ascending list
+// of distinct selected rows (padded with -1 to min(K, N) slots).
+static size_t fused_sel_bytes(int64_t N, int64_t K) {
+  return round_up(llp::select_workspace_bytes(N, K), 256);
+}
+
+size_t fused_logp_fwd_indexed_workspace_bytes(int64_t N, int64_t V, int64_t K) {
+  if (N <= 0 || K <= 0 || V < 1 || N > kLim31 || V > kLim31 || K > kLim31) return 0;
+  const int64_t Kc = K < N ? K : N;
+  return fused_sel_bytes(N, K) + static_cast<size_t>(2 * cdiv(V, llp::kLogitsSplit) * Kc) * sizeof(float);
+}
+
+size_t fused_logp_bwd_indexed_workspace_bytes(int64_t N, int64_t K) {
+  if (N <= 0 || N > kLim31 || K < 0 || K > kLim31) return 0;
+  return fused_sel_bytes(N, K);
+}
+
+int fused_logp_fwd_indexed(const void* logits, int dtype, int64_t N, int64_t V, const int64_t* targets,
+                           int64_t ignore_index, const int64_t* indices, int64_t K, float* out_logp,
+                           float* out_row_max, float* out_log_sum, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  int st = fused_check(logits, dtype, N, V, targets);
+  if (st != LLP_OK) return st;
+  if (K < 0 || K > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (N == 0 || K == 0) return LLP_OK;  // nothing selected: outputs untouched
+  if (indices == nullptr || out_logp == nullptr || out_row_max == nullptr || out_log_sum == nullptr ||
+      workspace == nullptr)
+    return LLP_ERR_NULL_POINTER;
+  if (!aligned(indices, 8) || !aligned(out_logp, 4) || !aligned(out_row_max, 4) || !aligned(out_log_sum, 4) ||
+      !aligned(workspace, 16))
+    return LLP_ERR_MISALIGNED;
+  if (workspace_bytes < fused_logp_fwd_indexed_workspace_bytes(N, V, K)) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  llp::RowSelection sel;
+  if (llp::build_row_selection(reinterpret_cast<const long long*>(indices), K, static_cast<int>(N), ws, &sel, s) !=
+      cudaSuccess)
+    return fail_cuda(__LINE__);
+  const cudaError_t e = llp::launch_logits_fwd(
+      logits, dtype, sel.K, sel.rows, static_cast<int>(V), reinterpret_cast<const long long*>(targets), ignore_index,
+      reinterpret_cast<float*>(ws + fused_sel_bytes(N, K)), out_logp, out_row_max, out_log_sum,
+      fused_vec_ok(logits, dtype, V), s);
+  return e == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
+}
+
+int fused_logp_bwd_indexed(const float* grad_logp, const float* row_max, const float* log_sum, const void* logits,
+                           int dtype, int64_t N, int64_t V, const int64_t* targets, int64_t ignore_index,
+                           const int64_t* indices, int64_t K, void* grad_logits, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  int st = fused_check(logits, dtype, N, V, targets);
+  if (st != LLP_OK) return st;
+  if (K < 0 || K > kLim31) return LLP_ERR_BAD_SHAPE;
+  if (N == 0) return LLP_OK;
+  if (grad_logp == nullptr || row_max == nullptr || log_sum == nullptr || grad_logits == nullptr ||
+      workspace == nullptr || (K > 0 && indices == nullptr))
+    return LLP_ERR_NULL_POINTER;
+  const uintptr_t es = dtype == FUSED_LOGP_DTYPE_F32 ? 4 : 2;
+  if (!aligned(grad_logp, 4) || !aligned(row_max, 4) || !aligned(log_sum, 4) || !aligned(grad_logits, es) ||
+      !aligned(workspace, 16) || (K > 0 && !aligned(indices, 8)))
+    return LLP_ERR_MISALIGNED;
+  if (workspace_bytes < fused_logp_bwd_indexed_workspace_bytes(N, K)) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInit* dev = nullptr;
+  if ((st = init_device(&dev)) != LLP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  llp::RowSelection sel;
+  if (llp::build_row_selection(reinterpret_cast<const long long*>(indices), K, static_cast<int>(N), workspace, &sel,
+                               s) != cudaSuccess)
+    return fail_cuda(__LINE__);
+  const bool vec = fused_vec_ok(logits, dtype, V) && fused_vec_ok(grad_logits, dtype, V);
+  const cudaError_t e = llp::launch_logits_bwd(logits, dtype, static_cast<int>(N), static_cast<int>(V),
+                                               reinterpret_cast<const long long*>(targets), ignore_index, grad_logp,
+                                               row_max, log_sum, sel.mask, grad_logits, vec, s);
   return e == cudaSuccess ? LLP_OK : fail_cuda(__LINE__);
 }
 

@@ -140,18 +140,20 @@ cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w
 cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const CUtensorMap& tm_out,
                                const GradGemmParams& p, long long units, const LaunchCaps& caps, cudaStream_t s);
 // Logits-input fused log-prob (logits.cu).  dtype: kDtypeBF16, kDtypeF32 or kDtypeF16.
-// `part` holds 2 * ceil(V / kLogitsSplit) * N floats.  `vec` = rows are 16-byte
-// aligned (base and row pitch), so 16-byte loads and stores may be used.
+// The forward works on P row slots: slot j is row rows[j] (row j when rows is
+// null; -1 = padding); `part` holds 2 * ceil(V / kLogitsSplit) * P floats.  The
+// backward writes all N rows, a zero row where `mask` (optional) is 0.  `vec` =
+// rows are 16-byte aligned (base and row pitch), so 16-byte loads and stores may be used.
 constexpr int kDtypeBF16 = 0;
 constexpr int kDtypeF32 = 1;
 constexpr int kDtypeF16 = 2;
 constexpr int kLogitsSplit = 16384;  // vocab elements per CTA (fixed: depends on nothing)
-cudaError_t launch_logits_fwd(const void* z, int dtype, int N, int V, const long long* targets,
+cudaError_t launch_logits_fwd(const void* z, int dtype, int P, const int* rows, int V, const long long* targets,
                               long long ignore_index, float* part, float* logp, float* row_max, float* log_sum,
                               bool vec, cudaStream_t s);
 cudaError_t launch_logits_bwd(const void* z, int dtype, int N, int V, const long long* targets,
                               long long ignore_index, const float* grad_logp, const float* row_max,
-                              const float* log_sum, void* grad, bool vec, cudaStream_t s);
+                              const float* log_sum, const unsigned char* mask, void* grad, bool vec, cudaStream_t s);
 
 // Row selection for the indexed variants (indexed.cu): the index list becomes a
 // byte mask over N rows and the selected rows, in ascending order, padded with

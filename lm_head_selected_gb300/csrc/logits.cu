@@ -202,8 +202,12 @@ __device__ __forceinline__ void block_merge(float& m, float& s, float* sm_m, flo
 // the thread's (max, sum) pair, so few registers are live and 8 CTAs per SM
 // keep many loads in flight.
 template <int DT, bool VEC>
+// Items are (slot, split) over P row slots: slot j is row rows[j] (row j when
+// rows is null; a slot of -1 is padding and does nothing); partials go to
+// [split][j].
 __global__ void __launch_bounds__(kLThreads, kLMinBlocks) logits_split_kernel(const typename Vec<DT>::T* __restrict__ z,
-                                                                    int N, int V, int S, float* __restrict__ part_m,
+                                                                    int V, int S, int P, const int* __restrict__ rows,
+                                                                    float* __restrict__ part_m,
                                                                     float* __restrict__ part_s) {
   using VV = Vec<DT>;
   constexpr int W = VV::W;
@@ -211,8 +215,10 @@ __global__ void __launch_bounds__(kLThreads, kLMinBlocks) logits_split_kernel(co
   constexpr int CHUNK = ITERS < kLChunk ? ITERS : kLChunk;
   __shared__ float sm_m[kLThreads / 32], sm_s[kLThreads / 32];
   const long long cta = blockIdx.x;
-  const int row = static_cast<int>(cta / S);
-  const int split = static_cast<int>(cta - static_cast<long long>(row) * S);
+  const int j = static_cast<int>(cta / S);
+  const int split = static_cast<int>(cta - static_cast<long long>(j) * S);
+  const int row = rows != nullptr ? rows[j] : j;
+  if (row < 0) return;  // padding slot (block-uniform)
   const int v0 = split * kLogitsSplit;
   const typename VV::T* zr = z + static_cast<size_t>(row) * V;
   float m = -INFINITY, s = 0.f;
@@ -249,19 +255,22 @@ __global__ void __launch_bounds__(kLThreads, kLMinBlocks) logits_split_kernel(co
   }
   block_merge(m, s, sm_m, sm_s);
   if (threadIdx.x == 0) {
-    part_m[static_cast<size_t>(split) * N + row] = m;
-    part_s[static_cast<size_t>(split) * N + row] = s;
+    part_m[static_cast<size_t>(split) * P + j] = m;
+    part_s[static_cast<size_t>(split) * P + j] = s;
   }
 }
 
 template <int DT>
-__global__ void __launch_bounds__(256) logits_merge_kernel(const typename Vec<DT>::T* __restrict__ z, int N, int V,
-                                                           int S, const long long* __restrict__ targets,
+__global__ void __launch_bounds__(256) logits_merge_kernel(const typename Vec<DT>::T* __restrict__ z, int P, int V,
+                                                           int S, const int* __restrict__ rows,
+                                                           const long long* __restrict__ targets,
                                                            long long ignore_index, const float* __restrict__ part_m,
                                                            const float* __restrict__ part_s, float* __restrict__ logp,
                                                            float* __restrict__ row_max, float* __restrict__ log_sum) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= P) return;
+  const int n = rows != nullptr ? rows[j] : j;
+  if (n < 0) return;  // padding slot
   const long long t = targets[n];
   if (!tgt_ok(t, V, ignore_index)) {
     logp[n] = 0.f;
@@ -270,10 +279,10 @@ __global__ void __launch_bounds__(256) logits_merge_kernel(const typename Vec<DT
     return;
   }
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[static_cast<size_t>(s) * N + n]);
+  for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[static_cast<size_t>(s) * P + j]);
   float Ssum = 0.f;
   for (int s = 0; s < S; ++s) {
-    const size_t i = static_cast<size_t>(s) * N + n;
+    const size_t i = static_cast<size_t>(s) * P + j;
     Ssum += part_s[i] * exp2f((part_m[i] - M) * kLog2eL);
   }
   const float ls = logf(Ssum);
@@ -290,6 +299,7 @@ __global__ void __launch_bounds__(kLThreads) logits_grad_kernel(const typename V
                                                                 const float* __restrict__ grad_logp,
                                                                 const float* __restrict__ row_max,
                                                                 const float* __restrict__ log_sum,
+                                                                const unsigned char* __restrict__ mask,
                                                                 typename Vec<DT>::T* __restrict__ grad) {
   using VV = Vec<DT>;
   constexpr int W = VV::W;
@@ -301,7 +311,8 @@ __global__ void __launch_bounds__(kLThreads) logits_grad_kernel(const typename V
   const typename VV::T* zr = z + static_cast<size_t>(row) * V;
   typename VV::T* gr = grad + static_cast<size_t>(row) * V;
   const long long t = targets[row];
-  const bool ok = tgt_ok(t, V, ignore_index);
+  // a row outside the selection (mask given and 0) gets a zero gradient row
+  const bool ok = tgt_ok(t, V, ignore_index) && (mask == nullptr || mask[row] != 0);
   const float g = ok ? grad_logp[row] : 0.f;
   const float m = ok ? row_max[row] : 0.f;
   const float ls = ok ? log_sum[row] : 0.f;
@@ -334,64 +345,68 @@ __global__ void __launch_bounds__(kLThreads) logits_grad_kernel(const typename V
 }
 
 template <int DT>
-cudaError_t launch_fwd_dt(const void* z, int N, int V, const long long* targets, long long ignore_index, float* part,
-                          float* logp, float* row_max, float* log_sum, bool vec, cudaStream_t s) {
+cudaError_t launch_fwd_dt(const void* z, int P, const int* rows, int V, const long long* targets,
+                          long long ignore_index, float* part, float* logp, float* row_max, float* log_sum, bool vec,
+                          cudaStream_t s) {
   using T = typename Vec<DT>::T;
   const int S = (V + kLogitsSplit - 1) / kLogitsSplit;
   float* pm = part;
-  float* ps = part + static_cast<size_t>(S) * N;
-  const long long items = static_cast<long long>(N) * S;
+  float* ps = part + static_cast<size_t>(S) * P;
+  const long long items = static_cast<long long>(P) * S;
   if (vec)
-    logits_split_kernel<DT, true><<<static_cast<unsigned>(items), kLThreads, 0, s>>>(static_cast<const T*>(z), N, V,
-                                                                                    S, pm, ps);
+    logits_split_kernel<DT, true><<<static_cast<unsigned>(items), kLThreads, 0, s>>>(static_cast<const T*>(z), V, S,
+                                                                                    P, rows, pm, ps);
   else
-    logits_split_kernel<DT, false><<<static_cast<unsigned>(items), kLThreads, 0, s>>>(static_cast<const T*>(z), N, V,
-                                                                                     S, pm, ps);
+    logits_split_kernel<DT, false><<<static_cast<unsigned>(items), kLThreads, 0, s>>>(static_cast<const T*>(z), V, S,
+                                                                                     P, rows, pm, ps);
   cudaError_t e = launch_result();
   if (e != cudaSuccess) return e;
-  logits_merge_kernel<DT><<<(N + 255) / 256, 256, 0, s>>>(static_cast<const T*>(z), N, V, S, targets, ignore_index, pm,
-                                                          ps, logp, row_max, log_sum);
+  logits_merge_kernel<DT><<<(P + 255) / 256, 256, 0, s>>>(static_cast<const T*>(z), P, V, S, rows, targets,
+                                                          ignore_index, pm, ps, logp, row_max, log_sum);
   return launch_result();
 }
 
 template <int DT>
 cudaError_t launch_bwd_dt(const void* z, int N, int V, const long long* targets, long long ignore_index,
-                          const float* grad_logp, const float* row_max, const float* log_sum, void* grad, bool vec,
-                          cudaStream_t s) {
+                          const float* grad_logp, const float* row_max, const float* log_sum,
+                          const unsigned char* mask, void* grad, bool vec, cudaStream_t s) {
   using T = typename Vec<DT>::T;
   const int S = (V + kLogitsSplit - 1) / kLogitsSplit;
   const long long ctas = static_cast<long long>(N) * S;
   if (vec)
     logits_grad_kernel<DT, true><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(
-        static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, static_cast<T*>(grad));
+        static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, mask,
+        static_cast<T*>(grad));
   else
     logits_grad_kernel<DT, false><<<static_cast<unsigned>(ctas), kLThreads, 0, s>>>(
-        static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, static_cast<T*>(grad));
+        static_cast<const T*>(z), N, V, S, targets, ignore_index, grad_logp, row_max, log_sum, mask,
+        static_cast<T*>(grad));
   return launch_result();
 }
 
 }  // namespace
 
-cudaError_t launch_logits_fwd(const void* z, int dtype, int N, int V, const long long* targets,
+cudaError_t launch_logits_fwd(const void* z, int dtype, int P, const int* rows, int V, const long long* targets,
                               long long ignore_index, float* part, float* logp, float* row_max, float* log_sum,
                               bool vec, cudaStream_t s) {
   if (dtype == kDtypeF16)
-    return launch_fwd_dt<kDtypeF16>(z, N, V, targets, ignore_index, part, logp, row_max, log_sum, vec, s);
-  return dtype == kDtypeBF16 ? launch_fwd_dt<kDtypeBF16>(z, N, V, targets, ignore_index, part, logp, row_max,
+    return launch_fwd_dt<kDtypeF16>(z, P, rows, V, targets, ignore_index, part, logp, row_max, log_sum, vec, s);
+  return dtype == kDtypeBF16 ? launch_fwd_dt<kDtypeBF16>(z, P, rows, V, targets, ignore_index, part, logp, row_max,
                                                          log_sum, vec, s)
-                             : launch_fwd_dt<kDtypeF32>(z, N, V, targets, ignore_index, part, logp, row_max, log_sum,
-                                                        vec, s);
+                             : launch_fwd_dt<kDtypeF32>(z, P, rows, V, targets, ignore_index, part, logp, row_max,
+                                                        log_sum, vec, s);
 }
 
 cudaError_t launch_logits_bwd(const void* z, int dtype, int N, int V, const long long* targets,
                               long long ignore_index, const float* grad_logp, const float* row_max,
-                              const float* log_sum, void* grad, bool vec, cudaStream_t s) {
+                              const float* log_sum, const unsigned char* mask, void* grad, bool vec,
+                              cudaStream_t s) {
   if (dtype == kDtypeF16)
-    return launch_bwd_dt<kDtypeF16>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum, grad, vec, s);
+    return launch_bwd_dt<kDtypeF16>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum, mask, grad, vec, s);
   return dtype == kDtypeBF16 ? launch_bwd_dt<kDtypeBF16>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum,
-                                                         grad, vec, s)
+                                                         mask, grad, vec, s)
                              : launch_bwd_dt<kDtypeF32>(z, N, V, targets, ignore_index, grad_logp, row_max, log_sum,
-                                                        grad, vec, s);
+                                                        mask, grad, vec, s);
 }
 
 }  // namespace llp

@@ -7,7 +7,7 @@ targets int64 with the logits' leading shape.
 from __future__ import annotations
 
 import ctypes
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -72,6 +72,64 @@ def fused_logp_bwd(grad_logp: torch.Tensor, row_max: torch.Tensor, log_sum: torc
                             _ptr(targets), int(ignore_index), _ptr(grad),
                             ctypes.c_void_p(torch.cuda.current_stream(logits.device).cuda_stream))
     _lib.check("fused_logp_bwd", st)
+    return grad
+
+
+def _indices(indices: torch.Tensor, device) -> torch.Tensor:
+    if not isinstance(indices, torch.Tensor) or indices.dtype != torch.int64 or indices.device != device:
+        raise TypeError("indices must be an int64 tensor on the logits' device")
+    return indices.reshape(-1).contiguous()
+
+
+@on_tensor_device
+def fused_logp_fwd_indexed(logits: torch.Tensor, targets: torch.Tensor, indices: torch.Tensor,
+                           ignore_index: int = IGNORE_INDEX,
+                           out: Optional[Tuple[torch.Tensor, torch.Tensor, torch.Tensor]] = None):
+    """Forward on the rows named by ``indices`` (duplicates count once, out of range
+    ignored).  Selected entries of (logp, row_max, log_sum) get the dense forward's
+    values; the others keep their contents (new buffers start as 0 / -inf / 0)."""
+    _check(logits, targets)
+    N, V = logits.shape
+    dev = logits.device
+    idx = _indices(indices, dev)
+    if out is None:
+        logp = torch.zeros(N, dtype=torch.float32, device=dev)
+        row_max = torch.full((N,), float("-inf"), dtype=torch.float32, device=dev)
+        log_sum = torch.zeros(N, dtype=torch.float32, device=dev)
+    else:
+        logp, row_max, log_sum = out
+    lib = _lib.load()
+    K = idx.numel()
+    ws = torch.empty(max(int(lib.fused_logp_fwd_indexed_workspace_bytes(N, V, K)), 1), dtype=torch.uint8, device=dev)
+    st = lib.fused_logp_fwd_indexed(_ptr(logits), _DTYPES[logits.dtype], N, V, _ptr(targets), int(ignore_index),
+                                    _ptr(idx), K, _ptr(logp), _ptr(row_max), _ptr(log_sum), _ptr(ws), ws.numel(),
+                                    ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    _lib.check("fused_logp_fwd_indexed", st)
+    return logp, row_max, log_sum
+
+
+@on_tensor_device
+def fused_logp_bwd_indexed(grad_logp: torch.Tensor, row_max: torch.Tensor, log_sum: torch.Tensor,
+                           logits: torch.Tensor, targets: torch.Tensor, indices: torch.Tensor,
+                           ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
+    """grad_logits [N, V] of sum over the selected rows of grad_logp * logp: rows
+    not selected are zero."""
+    _check(logits, targets)
+    N, V = logits.shape
+    dev = logits.device
+    idx = _indices(indices, dev)
+    for name, t in (("grad_logp", grad_logp), ("row_max", row_max), ("log_sum", log_sum)):
+        if t.dtype != torch.float32 or t.shape != (N,) or t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 [N] tensor on the logits' device")
+    grad = torch.empty_like(logits)
+    lib = _lib.load()
+    K = idx.numel()
+    ws = torch.empty(max(int(lib.fused_logp_bwd_indexed_workspace_bytes(N, K)), 1), dtype=torch.uint8, device=dev)
+    st = lib.fused_logp_bwd_indexed(_ptr(grad_logp), _ptr(row_max), _ptr(log_sum), _ptr(logits),
+                                    _DTYPES[logits.dtype], N, V, _ptr(targets), int(ignore_index), _ptr(idx), K,
+                                    _ptr(grad), _ptr(ws), ws.numel(),
+                                    ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    _lib.check("fused_logp_bwd_indexed", st)
     return grad
 
 

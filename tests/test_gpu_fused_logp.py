@@ -111,3 +111,29 @@ def test_autograd_leading_shape():
     g_ref = lo.backward(gl.double().numpy(), z.double().numpy(), t.numpy())
     _close("grad via autograd", zd.grad.reshape(60, 1000), g_ref, 1e-5, 1e-4)
     assert math.isfinite(float(out.sum()))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_indexed_rows(dtype):
+    """Row subsets ("recursive deterministic LogP autograd on B200", Indexed semantics):
+    selected rows equal the dense op bitwise, other outputs stay untouched, and the
+    gradient rows not selected are zero."""
+    import lm_head_selected_gb300 as llp
+    z, t, gl = _problem(70, 20000, dtype, seed=21)
+    zd, td, gd = z.cuda(), t.cuda(), gl.cuda()
+    lp0, m0, ls0 = llp.fused_logp_fwd(zd, td)
+    g0 = llp.fused_logp_bwd(gd, m0, ls0, zd, td)
+    idx = torch.tensor([3, 9, 9, 69, 0, 70, -1, 1], dtype=torch.int64, device="cuda")
+    rows = sorted({3, 9, 69, 0, 1})
+    sentinel = torch.full((70,), 123.0, device="cuda")
+    out = (sentinel.clone(), sentinel.clone(), sentinel.clone())
+    lp, m, ls = llp.fused_logp_fwd_indexed(zd, td, idx, out=out)
+    r = torch.tensor(rows, device="cuda")
+    assert torch.equal(lp[r], lp0[r]) and torch.equal(m[r], m0[r]) and torch.equal(ls[r], ls0[r])
+    others = torch.tensor(sorted(set(range(70)) - set(rows)), device="cuda")
+    assert torch.all(lp[others] == 123.0) and torch.all(m[others] == 123.0)
+    g = llp.fused_logp_bwd_indexed(gd, m0, ls0, zd, td, idx)
+    assert torch.equal(g[r], g0[r])
+    assert torch.all(g[others] == 0)
+    g_none = llp.fused_logp_bwd_indexed(gd, m0, ls0, zd, td, idx[:0])
+    assert torch.all(g_none == 0)
