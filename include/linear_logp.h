@@ -31,9 +31,10 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers into the current device's
- *     memory, row-major and contiguous.  bf16 tensors are passed as raw
- *     16-bit storage (void*).  The caller owns every buffer; the library
- *     allocates nothing and keeps no per-call state.
+ *     memory, row-major and contiguous.  16-bit tensors (bf16; IEEE fp16 for
+ *     the *_f16 entry points) are passed as raw storage (void*).  The caller
+ *     owns every buffer; the library allocates nothing and keeps no per-call
+ *     state (the one exception, linear_logp_fwd_noalloc, says so below).
  *   - `stream` is a cudaStream_t of the current device (NULL = legacy default
  *     stream).  Work is enqueued on it; the library never synchronises.  A
  *     thread with no current context gets the current device's primary one.
