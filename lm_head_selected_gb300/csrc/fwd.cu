@@ -52,7 +52,6 @@ struct FwdCfg {
   static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_last(); }
   static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
   static constexpr bool DYNAMIC = false;
-  static constexpr bool GROUPED = false;
   static __device__ __forceinline__ int* sched_counter(const Params&) { return nullptr; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
@@ -74,7 +73,6 @@ struct FwdCfg {
     ui.kb0 = 0;
     ui.nkb = (p.D + BK - 1) / BK;
     ui.bn = BN;
-    ui.which = 0;
     return ui;
   }
 
