@@ -29,7 +29,11 @@ constexpr float kLog2eL = 1.4426950408889634f;
 // Split-kernel shape, from a sweep at N=16384, V=131072, bf16 (0.712 ms for
 // the split pass against 1.09 ms with 8-vector chunks at 3 CTAs per SM):
 // 4 vectors per load batch, registers bounded so that 8 CTAs fit on an SM.
-constexpr int kLChunk = 4;
+constexpr int kLChunk = 4;  // the same in the aligned and the element-wise path: a row's
+                             // summation order must not depend on its address
+#ifndef LLP_PACKED_MAX
+#define LLP_PACKED_MAX 1  // chunk maximum on packed 16-bit pairs
+#endif
 constexpr int kLMinBlocks = 8;
 
 
@@ -89,6 +93,18 @@ struct Vec<kDtypeBF16> {
     *reinterpret_cast<uint4*>(p) = r;
   }
   static __device__ __forceinline__ void store1(T* p, float v) { *p = __float2bfloat16_rn(v); }
+  // Maximum of n packed vectors, taken on bf16 pairs (exact: the result is one of the elements).
+  template <int NV>
+  static __device__ __forceinline__ float max_of(const uint4 (&r)[NV]) {
+    __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&r[0].x);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+      for (int k = (i == 0 ? 1 : 0); k < 4; ++k) m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    }
+    return fmaxf(__low2float(m), __high2float(m));
+  }
 };
 template <>
 struct Vec<kDtypeF32> {
@@ -118,6 +134,14 @@ struct Vec<kDtypeF32> {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
   static __device__ __forceinline__ void store1(T* p, float v) { *p = v; }
+  template <int NV>
+  static __device__ __forceinline__ float max_of(const uint4 (&r)[NV]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) m = fmaxf(fmaxf(fmaxf(m, __uint_as_float(r[i].x)), __uint_as_float(r[i].y)),
+                                           fmaxf(__uint_as_float(r[i].z), __uint_as_float(r[i].w)));
+    return m;
+  }
 };
 
 template <>
@@ -161,6 +185,17 @@ struct Vec<kDtypeF16> {
     *reinterpret_cast<uint4*>(p) = r;
   }
   static __device__ __forceinline__ void store1(T* p, float v) { *p = __float2half_rn(v); }
+  template <int NV>
+  static __device__ __forceinline__ float max_of(const uint4 (&r)[NV]) {
+    __half2 m = *reinterpret_cast<const __half2*>(&r[0].x);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+      for (int k = (i == 0 ? 1 : 0); k < 4; ++k) m = __hmax2(m, *reinterpret_cast<const __half2*>(&w[k]));
+    }
+    return fmaxf(__low2float(m), __high2float(m));
+  }
 };
 
 // Merge (m, s) pairs: s is a sum of exp(x - m).
@@ -231,13 +266,18 @@ __global__ void __launch_bounds__(kLThreads, kLMinBlocks) logits_split_kernel(co
       // n_valid <= 0: nothing is read and every element is -inf
       raw[i] = VV::load_raw(zr + (v < V ? v : 0), V - v, VEC);
     }
-    float cm = -INFINITY;
+    float cm;
+    if (LLP_PACKED_MAX) {
+      cm = VV::template max_of<CHUNK>(raw);
+    } else {
+      cm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < CHUNK; ++i) {
-      float x[W];
-      VV::unpack(raw[i], x);
+      for (int i = 0; i < CHUNK; ++i) {
+        float x[W];
+        VV::unpack(raw[i], x);
 #pragma unroll
-      for (int k = 0; k < W; ++k) cm = fmaxf(cm, x[k]);
+        for (int k = 0; k < W; ++k) cm = fmaxf(cm, x[k]);
+      }
     }
     if (cm == -INFINITY) continue;
     // x - cm first (exact near the maximum), so a large constant logit shift
