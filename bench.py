@@ -71,9 +71,9 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by hash).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "a3ab69940f6dff34",
-    "bytes_per_launch": {"fwd_partials": 2639398400 + 37245952, "dlogits": 5613756160 + 4260891136,
-                         "grad_hidden": 20002212864 + 699163136, "grad_weight": 13128675072 + 698261248},
+    "sources_sha": "233c24655fa5f8e3",
+    "bytes_per_launch": {"fwd_partials": 4035661056 + 37029120, "dlogits": 9825680640 + 4266166016,
+                         "grad_hidden": 28203747328 + 700253184, "grad_weight": 16824336896 + 697069312},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
