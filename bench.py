@@ -71,9 +71,9 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by hash).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "233c24655fa5f8e3",
-    "bytes_per_launch": {"fwd_partials": 4035661056 + 37029120, "dlogits": 9825680640 + 4266166016,
-                         "grad_hidden": 28203747328 + 700253184, "grad_weight": 16824336896 + 697069312},
+    "sources_sha": "6b9d2e1731d0bef4",
+    "bytes_per_launch": {"fwd_partials": 2695001088 + 37051648, "dlogits": 7399388416 + 4267767552,
+                         "grad_hidden": 25871829504 + 695279872, "grad_weight": 19211192064 + 701426176},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")

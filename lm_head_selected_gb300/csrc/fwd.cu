@@ -158,60 +158,93 @@ struct FwdCfg {
   }
 };
 
-// A block merges 32 rows: lane l of every warp serves row n0 + l, and the 8
-// warps split the vocab-split range, so every partial load is a coalesced
-// 128-byte row segment.  The maximum is combined across warps (exact in any
-// order); the terms exp(m_s - M) are staged in shared memory and lane l of warp
-// 0 folds them in ascending split order with fused multiply-adds, so a row's
-// sum is the same sequence of roundings whatever N or the grid is.
-constexpr int kMergeRows = 32;   // rows per 256-thread block
-constexpr int kMergeWarps = 8;   // warps sharing a row's splits
-constexpr int kMergeChunk = 64;  // splits staged per pass
+// A block merges 32 rows: lane l of every warp serves row n0 + l, and warp w
+// holds a contiguous run of kMergeHeld splits of each round of kMergeRound
+// splits in registers, so every partial load is a coalesced 128-byte row
+// segment and all of a warp's loads are in flight at once.  The maximum is
+// combined across warps (exact in any order).  The sum is one chain of fused
+// multiply-adds in ascending split order: warp 0 folds its run, hands the
+// running sum to warp 1 through shared memory, and so on, so a row's sum is the
+// same sequence of roundings whatever N or the grid is.  At small N a single
+// block does all the work, and its time is the number of dependent round trips
+// to memory: one per round (two when the splits need more than one round).
+constexpr int kMergeRows = 32;                           // rows per 256-thread block
+constexpr int kMergeWarps = 8;                           // warps sharing a row's splits
+constexpr int kMergeHeld = 32;                           // splits a warp holds per round
+constexpr int kMergeRound = kMergeWarps * kMergeHeld;  // splits per round
 
 struct MergeSmem {
   float red[kMergeWarps][kMergeRows];
-  float ps[kMergeChunk][kMergeRows];
-  float ex[kMergeChunk][kMergeRows];
+  float carry[kMergeRows];
 };
 
-// Returns (M, S) of row n in lanes of warp 0 (other warps: undefined).  All
+// Loads warp w's run of round r0: m (and s when `with_s`) of splits
+// r0 + w * kMergeHeld + k; splits past the end read as m = -inf, s = 0.
+__device__ __forceinline__ void merge_load_run(const FwdParams& p, int n, int r0, int w, bool with_s,
+                                               float (&mv)[kMergeHeld], float (&sv)[kMergeHeld]) {
+#pragma unroll
+  for (int k = 0; k < kMergeHeld; ++k) {
+    const int s = r0 + w * kMergeHeld + k;
+    const size_t i = static_cast<size_t>(s) * p.N + n;
+    mv[k] = s < p.num_splits ? p.part_m[i] : -INFINITY;
+    if (with_s) sv[k] = s < p.num_splits ? p.part_s[i] : 0.f;
+  }
+}
+
+// Returns (M, S) of row n in every thread of lane n - n0 (all warps).  All
 // threads of the block must call it.
 __device__ __forceinline__ void merge_splits_block(const FwdParams& p, int n, MergeSmem& sm, float& M, float& S) {
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   const bool valid = n < p.N;
+  const int ns = p.num_splits;
+  const bool held = ns <= kMergeRound;  // one round: the first loads serve both passes
+  float mv[kMergeHeld], sv[kMergeHeld];
   float mx = -INFINITY;
-  if (valid)
-    for (int s = w; s < p.num_splits; s += kMergeWarps) mx = fmaxf(mx, p.part_m[static_cast<size_t>(s) * p.N + n]);
+  for (int r0 = 0; r0 < ns; r0 += kMergeRound) {
+    if (valid) {
+      merge_load_run(p, n, r0, w, held, mv, sv);
+#pragma unroll
+      for (int k = 0; k < kMergeHeld; ++k) mx = fmaxf(mx, mv[k]);
+    }
+  }
   sm.red[w][lane] = mx;
+  if (w == 0) sm.carry[lane] = 0.f;
   __syncthreads();
   M = sm.red[0][lane];
 #pragma unroll
   for (int k = 1; k < kMergeWarps; ++k) M = fmaxf(M, sm.red[k][lane]);
-  S = 0.f;
-  for (int s0 = 0; s0 < p.num_splits; s0 += kMergeChunk) {
-    const int cnt = min(kMergeChunk, p.num_splits - s0);
-    if (valid)
-      for (int j = w; j < cnt; j += kMergeWarps) {
-        const size_t i = static_cast<size_t>(s0 + j) * p.N + n;
-        sm.ps[j][lane] = p.part_s[i];
-        sm.ex[j][lane] = exp2f((p.part_m[i] - M) * kLog2e);
+  for (int r0 = 0; r0 < ns; r0 += kMergeRound) {
+    if (valid) {
+      if (!held) merge_load_run(p, n, r0, w, true, mv, sv);
+#pragma unroll
+      for (int k = 0; k < kMergeHeld; ++k) mv[k] = exp2f((mv[k] - M) * kLog2e);
+    }
+    for (int ww = 0; ww < kMergeWarps; ++ww) {
+      if (w == ww && valid) {
+        float acc = sm.carry[lane];
+#pragma unroll
+        for (int k = 0; k < kMergeHeld; ++k)
+          if (r0 + ww * kMergeHeld + k < ns) acc = __fmaf_rn(sv[k], mv[k], acc);
+        sm.carry[lane] = acc;
       }
-    __syncthreads();
-    if (w == 0 && valid)
-      for (int j = 0; j < cnt; ++j) S = __fmaf_rn(sm.ps[j][lane], sm.ex[j][lane], S);
-    __syncthreads();
+      __syncthreads();
+    }
   }
+  S = sm.carry[lane];
 }
 
 __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __restrict__ out_logp,
                                                         float* __restrict__ out_lse) {
   __shared__ MergeSmem sm;
   const int n = blockIdx.x * kMergeRows + (threadIdx.x & 31);
+  const bool mine = threadIdx.x < 32 && n < p.N;
+  // issued before the merge so that their latency overlaps it; zt is used only for valid targets
+  const long long t = mine ? p.targets[n] : 0;
+  const float zt = mine ? p.zt[n] : 0.f;
   float M, S;
   merge_splits_block(p, n, sm, M, S);
-  if (threadIdx.x >= 32 || n >= p.N) return;
-  const long long t = p.targets[n];
+  if (!mine) return;
   if (!target_valid(t, p.V, p.ignore_index)) {
     out_logp[n] = 0.f;
     out_lse[n] = -INFINITY;
@@ -219,7 +252,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdParams p, float* __re
   }
   const float ls = logf(S);
   out_lse[n] = M + ls;
-  out_logp[n] = (p.zt[n] - M) - ls;
+  out_logp[n] = (zt - M) - ls;
 }
 
 // Vocab-parallel shard statistics ("Fused Linear LogP", Tensor Parallel Vocab

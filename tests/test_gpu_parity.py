@@ -49,6 +49,8 @@ SHAPES = [
     (64, 128, 32832, False, False, 0, 0),  # two vocab K segments [32768, 64]
     (96, 2688, 4096, True, True, 2, 1),   # full Nemotron hidden size, 42 k-blocks
     (257, 512, 2048, False, True, 0, 0),  # three M tiles, the last with one row
+    (33, 64, 131073, False, True, 1, 0),  # 257 vocab splits: the split merge takes a second round of one split
+    (40, 64, 200000, True, False, 2, 1),  # 391 vocab splits, ragged last split
 ]
 
 
