@@ -408,7 +408,10 @@ def run_ours(args):
     fwd_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.steps
 
     # end to end through the public autograd API with pinned host inputs and a
-    # device-to-host read of the per-token log-probs every step
+    # device-to-host read of the per-token log-probs every step.  As in a training
+    # input pipeline, the next step's inputs are copied on a second stream while
+    # the current step computes: K steps time K host-to-device copies (the first
+    # step's before the timed region, one for a step after it inside).
     h_host = inp.hidden.pin_memory()
     t_host = inp.targets.pin_memory()
     g_host = inp.grad_logp.pin_memory()
@@ -416,28 +419,44 @@ def run_ours(args):
     out_host = torch.empty(N, dtype=torch.float32).pin_memory()
     w_param = w.detach().clone().requires_grad_(True)
     b_param = None if b is None else b.detach().clone().requires_grad_(True)
+    copy_stream = torch.cuda.Stream(dev)
 
-    def e2e_step():
+    def prefetch():
+        with torch.cuda.stream(copy_stream):
+            bufs = (h_host.to(dev, non_blocking=True), t_host.to(dev, non_blocking=True),
+                    g_host.to(dev, non_blocking=True),
+                    None if tau_host is None else tau_host.to(dev, non_blocking=True))
+        ready = torch.cuda.Event()
+        ready.record(copy_stream)
+        return bufs, ready
+
+    def e2e_step(staged):
+        bufs, ready = staged
+        stream.wait_event(ready)
+        for x in bufs:
+            if x is not None:
+                x.record_stream(stream)
+        nxt = prefetch()
         flush()
-        hd = h_host.to(dev, non_blocking=True).requires_grad_(True)
-        td = t_host.to(dev, non_blocking=True)
-        gd = g_host.to(dev, non_blocking=True)
-        taud = None if tau_host is None else tau_host.to(dev, non_blocking=True)
+        hd, td, gd, taud = bufs
+        hd.requires_grad_(True)
         w_param.grad = None
         if b_param is not None:
             b_param.grad = None
         lp = llp.linear_logp(hd, w_param, td, b_param, taud)
         lp.backward(gd)
         out_host.copy_(lp.detach(), non_blocking=True)
+        return nxt
 
+    staged = prefetch()
     for _ in range(3):
-        e2e_step()
+        staged = e2e_step(staged)
     barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        e2e_step()
+        staged = e2e_step(staged)
     t1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
@@ -475,7 +494,8 @@ def run_ours(args):
                          "tensor_peak_frac": 2.0 * N * V * D / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"]},
             "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "api": "lm_head_selected_gb300.linear_logp autograd, pinned host inputs"},
+                    "api": "lm_head_selected_gb300.linear_logp autograd, pinned host inputs",
+                    "copies": "next step's inputs copied on a second stream during the current step"},
             "cpu_baseline": cpu,
             "clocks": clk,
             "peaks": peaks,

@@ -285,6 +285,21 @@ void rec_mark(cudaStream_t s, int id) {
   ++g_rec.used;
 }
 
+// Row tiling of the two token-row GEMMs (forward logits, dlogits) for a batch of
+// N rows.  A batch that fits in one 128-row tile runs on single CTAs: in a CTA
+// pair the second CTA's 128 rows would all be padding, and single CTAs put
+// every SM on the weight stream.  Both tilings issue the same tensor-core MMAs
+// along K for every element, so a row's results do not depend on which ran.
+struct RowTiling {
+  bool single;
+  int unit_rows;   // rows per unit: kTileM single, kUnitM pair
+  int w_box_rows;  // rows of a weight tile each CTA loads
+};
+RowTiling row_tiling(int64_t N) {
+  const bool single = N <= llp::kTileM;
+  return {single, single ? llp::kTileM : llp::kUnitM, single ? llp::kTileN : llp::kBRows};
+}
+
 // Forward launch sequence on validated arguments (N > 0, workspace sized by fwd_layout).
 // With sh_max set, `weight` is a vocab shard whose row 0 is global id vocab_start,
 // and the shard's (max, sum, target logit) triple is written instead of logp / lse.
@@ -293,14 +308,15 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
              float* out_lse, uint8_t* ws, cudaStream_t s, int64_t vocab_start = 0, float* sh_max = nullptr,
              float* sh_se = nullptr, float* sh_tl = nullptr, bool f16 = false) {
   const FwdLayout L = fwd_layout(N, V);
+  const RowTiling T = row_tiling(N);
   CUtensorMap tm_h, tm_w;
   if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return fail_cuda(__LINE__);
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, T.w_box_rows, f16) != LLP_OK) return fail_cuda(__LINE__);
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
   p.V = static_cast<int>(V);
-  p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+  p.num_m = static_cast<int>(cdiv(N, T.unit_rows));
   p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
   p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
   p.group_m = llp::kGroupM;
@@ -317,7 +333,7 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.f16 = f16 ? 1 : 0;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   rec_mark(s, -1);
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return fail_cuda(__LINE__);
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s, T.single) != cudaSuccess) return fail_cuda(__LINE__);
   rec_mark(s, kKFwdPartials);
   if (sh_max != nullptr) {
     if (llp::launch_shard_stats(p, sh_max, sh_se, sh_tl, s) != cudaSuccess) return fail_cuda(__LINE__);
@@ -364,16 +380,17 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   int* sched = reinterpret_cast<int*>(ws + L.sched);  // zeroed by the dlogits kernel
 
   // B1: dlogits (+ grad_bias partials)
+  const RowTiling T = row_tiling(N);
   {
     CUtensorMap tm_h, tm_w;
     if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
-    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows, f16) != LLP_OK) return fail_cuda(__LINE__);
+    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, T.w_box_rows, f16) != LLP_OK) return fail_cuda(__LINE__);
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
     p.V = static_cast<int>(V);
     p.V_pad = static_cast<int>(V_pad);
-    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+    p.num_m = static_cast<int>(cdiv(N, T.unit_rows));
     p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
     p.group_m = llp::kGroupM;
     p.bias = bias;
@@ -393,7 +410,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     rec_mark(s, -1);
     CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
     if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32, f16) != LLP_OK) return fail_cuda(__LINE__);
-    if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s) != cudaSuccess) return fail_cuda(__LINE__);
+    if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s, T.single) != cudaSuccess)
+      return fail_cuda(__LINE__);
     rec_mark(s, kKDlogits);
   }
 
@@ -466,7 +484,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
 
   // B4: grad_bias
   if (want_gb) {
-    const int nblocks = static_cast<int>(cdiv(N, llp::kUnitM) * (llp::kUnitM / 32));
+    // the 32-row blocks the dlogits units covered (padding rows give zero sums)
+    const int nblocks = static_cast<int>(cdiv(N, T.unit_rows) * (T.unit_rows / 32));
     if (llp::launch_bias_sum(reinterpret_cast<const float*>(ws + L.gb_part), nblocks, static_cast<int>(V), grad_bias,
                              s) != cudaSuccess)
       return fail_cuda(__LINE__);
@@ -1157,16 +1176,17 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   if ((st = noalloc_scratch(&scratch)) != LLP_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  const RowTiling T = row_tiling(N);
   CUtensorMap tm_h, tm_w;
   if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return fail_cuda(__LINE__);
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, llp::kBRows) != LLP_OK) return fail_cuda(__LINE__);
+  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, T.w_box_rows) != LLP_OK) return fail_cuda(__LINE__);
 
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
   p.V = static_cast<int>(V);
-  p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+  p.num_m = static_cast<int>(cdiv(N, T.unit_rows));
   p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
   p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
   p.group_m = llp::kGroupM;
@@ -1183,7 +1203,8 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   p.f16 = 0;
 
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s) != cudaSuccess) return fail_cuda(__LINE__);
+  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s, T.single) != cudaSuccess)
+    return fail_cuda(__LINE__);
   if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return fail_cuda(__LINE__);
   return LLP_OK;
 }

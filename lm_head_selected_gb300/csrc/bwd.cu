@@ -66,15 +66,16 @@ __device__ __forceinline__ uint32_t pack16x2(bool f16, float a, float b) {
 // ----------------------------------------------------------------------------
 // B1: dlogits
 // ----------------------------------------------------------------------------
-template <bool HAS_BIAS>
+// PAIRED = false: single CTAs with 128-row tiles, for a batch that fits in one.
+template <bool HAS_BIAS, bool PAIRED = kPairMMA>
 struct DzCfg {
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
-  static constexpr bool PAIR = kPairMMA;
+  static constexpr bool PAIR = PAIRED;
   static constexpr int BN = kTileN;
   static constexpr int STAGES = PAIR ? kPairStages : 4;
   static constexpr int EXTRA_SMEM = kEpiSmemBytes;
-  static constexpr int UM = kUnitM;
+  static constexpr int UM = PAIR ? kUnitM : kTileM;
   using Params = DzParams;
 
   struct RowState {
@@ -358,12 +359,17 @@ cudaError_t bwd_setup(LaunchCaps* caps) {
   cudaError_t e;
   if ((e = setup_gemm<DzCfg<false>>(&caps->dz_groups[0])) != cudaSuccess) return e;
   if ((e = setup_gemm<DzCfg<true>>(&caps->dz_groups[1])) != cudaSuccess) return e;
+  if ((e = setup_gemm<DzCfg<false, false>>(&caps->dz_single[0])) != cudaSuccess) return e;
+  if ((e = setup_gemm<DzCfg<true, false>>(&caps->dz_single[1])) != cudaSuccess) return e;
   if ((e = setup_gemm<GradCfg<false, true>>(&caps->gh_groups)) != cudaSuccess) return e;
   return setup_gemm<GradCfg<true, true>>(&caps->gw_groups);
 }
 
 cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_dz_out,
-                           const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s) {
+                           const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s, bool single) {
+  if (single)
+    return p.bias ? launch_units<DzCfg<true, false>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_single[1], s)
+                  : launch_units<DzCfg<false, false>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_single[0], s);
   return p.bias ? launch_units<DzCfg<true>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_groups[1], s)
                 : launch_units<DzCfg<false>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_groups[0], s);
 }

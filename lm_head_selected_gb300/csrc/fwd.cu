@@ -28,16 +28,18 @@ __device__ __forceinline__ bool target_valid(long long t, int V, long long ignor
   return t != ignore_index && t >= 0 && t < static_cast<long long>(V);
 }
 
-template <bool HAS_BIAS>
+// PAIRED = false: single CTAs with 128-row tiles, used when the whole batch fits
+// in one of them (a pair's second CTA would hold only padding rows).
+template <bool HAS_BIAS, bool PAIRED = kPairMMA>
 struct FwdCfg {
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
-  static constexpr bool PAIR = kPairMMA;
+  static constexpr bool PAIR = PAIRED;
   static constexpr int BN = kTileN;
   static constexpr int STAGES = PAIR ? kPairStages : 4;
   static constexpr int EXTRA_SMEM = 0;
   static constexpr int TPS = kTilesPerSplit;
-  static constexpr int UM = kUnitM;
+  static constexpr int UM = PAIR ? kUnitM : kTileM;
   using Params = FwdParams;
 
   struct RowState {
@@ -322,8 +324,10 @@ cudaError_t launch_merge_shards(const float* mx, const float* se, const float* t
 
 cudaError_t fwd_setup(LaunchCaps* caps) {
   cudaError_t e = setup_gemm<FwdCfg<false>>(&caps->fwd_groups[0]);
-  if (e != cudaSuccess) return e;
-  return setup_gemm<FwdCfg<true>>(&caps->fwd_groups[1]);
+  if (e == cudaSuccess) e = setup_gemm<FwdCfg<true>>(&caps->fwd_groups[1]);
+  if (e == cudaSuccess) e = setup_gemm<FwdCfg<false, false>>(&caps->fwd_single[0]);
+  if (e == cudaSuccess) e = setup_gemm<FwdCfg<true, false>>(&caps->fwd_single[1]);
+  return e;
 }
 
 template <class Cfg>
@@ -334,7 +338,10 @@ static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, cons
 }
 
 cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,
-                                long long units, const LaunchCaps& caps, cudaStream_t s) {
+                                long long units, const LaunchCaps& caps, cudaStream_t s, bool single) {
+  if (single)
+    return p.bias ? launch_units<FwdCfg<true, false>>(tm_h, tm_w, p, units, caps.fwd_single[1], s)
+                  : launch_units<FwdCfg<false, false>>(tm_h, tm_w, p, units, caps.fwd_single[0], s);
   return p.bias ? launch_units<FwdCfg<true>>(tm_h, tm_w, p, units, caps.fwd_groups[1], s)
                 : launch_units<FwdCfg<false>>(tm_h, tm_w, p, units, caps.fwd_groups[0], s);
 }

@@ -51,7 +51,9 @@ constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 // found once per device; the persistent grids never exceed them.
 struct LaunchCaps {
   int fwd_groups[2];  // [has_bias]
+  int fwd_single[2];  // [has_bias], single-CTA forward for batches of at most kTileM rows
   int dz_groups[2];   // [has_bias]
+  int dz_single[2];   // [has_bias], single-CTA dlogits for batches of at most kTileM rows
   int gh_groups;
   int gw_groups;
 };
@@ -117,8 +119,10 @@ inline cudaError_t launch_result() { return note_cuda(cudaGetLastError()); }
 // Launchers (return the launch error, never synchronise).  `units` is the
 // number of work units; the grid is min(units, resident groups) groups.
 cudaError_t fwd_setup(LaunchCaps* caps);
+// single: 128-row single-CTA tiles (p.num_m counted in kTileM rows, W map box
+// kTileN rows) instead of 256-row CTA-pair tiles (kUnitM rows, box kBRows rows).
 cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,
-                                long long units, const LaunchCaps& caps, cudaStream_t s);
+                                long long units, const LaunchCaps& caps, cudaStream_t s, bool single);
 cudaError_t launch_fwd_merge(const FwdParams& p, float* out_logp, float* out_lse, cudaStream_t s);
 // Vocab-parallel shards: per-row (max, sum of exp(z - max), target logit or -inf)
 // of this shard, and the ascending-rank merge of R shards' triples.
@@ -134,7 +138,8 @@ cudaError_t bwd_setup(LaunchCaps* caps);
 // box 64 x 32), or the gradient (bf16, box 64 x 32) / its fp32 segment
 // partials ([nseg][rows][D], box 32 x 32 x 1).
 cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_dz_out,
-                           const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s);
+                           const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s,
+                           bool single);
 cudaError_t launch_grad_hidden(const CUtensorMap& tm_dz, const CUtensorMap& tm_w_mn, const CUtensorMap& tm_out,
                                const GradGemmParams& p, long long units, const LaunchCaps& caps, cudaStream_t s);
 cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& tm_h_mn, const CUtensorMap& tm_out,

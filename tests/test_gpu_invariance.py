@@ -48,6 +48,23 @@ def test_batch_invariance(pool, size):
     assert torch.equal(gh_s, gh[di]), "grad_hidden rows changed with the batch size"
 
 
+@pytest.mark.parametrize("size", [128, 129])
+def test_row_tiling_boundary(pool, size):
+    """Batches of at most 128 rows run the forward and dlogits GEMMs on single
+    CTAs with 128-row tiles, larger ones on CTA pairs with 256-row tiles; a row's
+    results must not change across that boundary."""
+    inp, d, logp, lse, gh = pool
+    gen = torch.Generator().manual_seed(1000 + size)
+    idx = torch.randperm(inp.N, generator=gen)[:size].sort().values
+    ds = to_device(inp.rows(idx))
+    lp_s, lse_s = gpu_fwd(ds)
+    gh_s, _, _ = gpu_bwd(ds, lse_s, need_weight=False)
+    check_device_status()
+    di = idx.cuda()
+    assert torch.equal(lp_s, logp[di]) and torch.equal(lse_s, lse[di])
+    assert torch.equal(gh_s, gh[di])
+
+
 def test_pool_matches_oracle_on_sampled_rows(pool):
     inp, d, logp, lse, gh = pool
     rows = list(range(0, inp.N, 16)) + [inp.N - 1]
