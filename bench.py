@@ -71,9 +71,9 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by hash).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "6b9d2e1731d0bef4",
-    "bytes_per_launch": {"fwd_partials": 2695001088 + 37051648, "dlogits": 7399388416 + 4267767552,
-                         "grad_hidden": 25871829504 + 695279872, "grad_weight": 19211192064 + 701426176},
+    "sources_sha": "217cbcc2a155e04e",
+    "bytes_per_launch": {"fwd_partials": 2169387264 + 37225728, "dlogits": 6398021376 + 4268878336,
+                         "grad_hidden": 24050236672 + 694915840, "grad_weight": 16667673088 + 701035264},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
