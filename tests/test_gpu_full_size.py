@@ -35,6 +35,29 @@ def _forward_properties(logp, lse, inp):
     assert torch.all(torch.isfinite(lse[valid])) and torch.all(torch.isneginf(lse[~valid]))
 
 
+def _zero_sum_identities(inp, gw, gb=None):
+    """Every valid row's dlogits sums to zero over the vocabulary (g/tau times one
+    minus the softmax's total), so at any size sum_v grad_W[v, :] = 0 and
+    sum_v grad_b[v] = 0.  Allowed slack: each bf16 element of grad_W carries at
+    most 2^-9 relative rounding (so a column sum may stray by that share of the
+    column's absolute sum, doubled here), plus 1e-4 of sum_n |g_n / tau_n| |h[n, d]|
+    for the fp32 softmax total (1 - sum_v p is about 1e-6 per row) and the fp32
+    accumulation.  A dropped term (the one-hot part, a vocab tile, a token
+    segment) breaks the identity by far more."""
+    valid = torch.as_tensor(oracle.valid_rows(inp.targets.numpy(), inp.V, inp.ignore_index))
+    gs = inp.grad_logp.double().abs()
+    if inp.temperature is not None:
+        gs = gs / inp.temperature.double()
+    gs = torch.where(valid, gs, torch.zeros_like(gs))
+    s1 = (gs[:, None] * inp.hidden.double().abs()).sum(0).cuda()
+    col = gw.double().sum(0)
+    mag = gw.double().abs().sum(0)
+    bad = col.abs() > 2.0 ** -8 * mag + 1e-4 * s1
+    assert not torch.any(bad), f"sum_v grad_W[v, d] != 0 for {int(bad.sum())} columns"
+    if gb is not None:
+        assert abs(float(gb.double().sum())) <= 1e-4 * float(gs.sum())
+
+
 def _sparse_targets(inp, active, seed):
     """Same inputs, but only `active` rows keep their target; the rest are ignored."""
     g = torch.Generator().manual_seed(seed)
@@ -74,6 +97,7 @@ def test_rl_head_fwd_bwd_full_size():
     check_backward(inp, gh, None, None, rows=rows)
     gh2, gw2, _ = gpu_bwd(d, lse)
     assert torch.equal(gh, gh2) and torch.equal(gw, gw2)
+    _zero_sum_identities(inp, gw)
     del gw, gw2, gh2
     sp = _sparse_targets(inp, 192, 3)
     ds = to_device(sp)
@@ -96,6 +120,7 @@ def test_train_step_full_size():
     check_forward(inp, logp, lse, rows=rows)
     check_backward(inp, gh, None, None, rows=rows)
     assert torch.all(torch.isfinite(gb))
+    _zero_sum_identities(inp, gw, gb)
     del gw, gh
     sp = _sparse_targets(inp, 128, 5)
     ds = to_device(sp)
@@ -121,6 +146,7 @@ def test_long_context_full_size():
     gh2, gw2, _ = gpu_bwd(d, lse2)
     assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
     assert torch.equal(gh, gh2) and torch.equal(gw, gw2)
+    _zero_sum_identities(inp, gw)
     del gw, gw2, gh, gh2
     # the shifted row agrees with its unshifted twin
     twin = inp.rows(torch.tensor([0]))
