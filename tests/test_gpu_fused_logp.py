@@ -110,7 +110,7 @@ def test_autograd_leading_shape():
     (out * gl.cuda().view(3, 20)).sum().backward()
     g_ref = lo.backward(gl.double().numpy(), z.double().numpy(), t.numpy())
     _close("grad via autograd", zd.grad.reshape(60, 1000), g_ref, 1e-5, 1e-4)
-    assert math.isfinite(float(out.sum()))
+    assert math.isfinite(float(out.detach().sum()))
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
@@ -137,3 +137,36 @@ def test_indexed_rows(dtype):
     assert torch.all(g[others] == 0)
     g_none = llp.fused_logp_bwd_indexed(gd, m0, ls0, zd, td, idx[:0])
     assert torch.all(g_none == 0)
+
+
+def test_full_size_benchmark_problem():
+    """The benchmark's problem and launch configuration (N=16384, V=131072, bf16
+    logits drawn as ``bench.py --op fused_logp`` draws them, plus ignored rows):
+    every row valid, sampled rows against the oracle, bitwise repeatable."""
+    import lm_head_selected_gb300 as llp
+    N, V = 16384, 131072
+    g = torch.Generator().manual_seed(1005)
+    z = (torch.randn(N, V, generator=g) * 3.0).to(torch.bfloat16)
+    t = torch.randint(0, V, (N,), generator=g)
+    gl = torch.randn(N, generator=g)
+    t[::97] = -100
+    zd, td, gd = z.cuda(), t.cuda(), gl.cuda()
+    logp, m, ls = llp.fused_logp_fwd(zd, td)
+    grad = llp.fused_logp_bwd(gd, m, ls, zd, td)
+    ok = torch.as_tensor(lo.valid_rows(t.numpy(), V, -100)).cuda()
+    assert torch.all(torch.isfinite(logp)) and torch.all(logp[ok] <= 0) and torch.all(logp[~ok] == 0)
+    assert torch.all(torch.isfinite(ls[ok])) and torch.all(torch.isneginf(m[~ok]))
+    assert torch.all(grad[~ok] == 0)
+    rows = sorted(set(torch.randperm(N, generator=torch.Generator().manual_seed(9))[:64].tolist()) | {0, 97, N - 1})
+    r = torch.tensor(rows)
+    zr, tr = z[r].double().numpy(), t[r].numpy()
+    lp_ref, m_ref, ls_ref = lo.forward(zr, tr)
+    okr = lo.valid_rows(tr, V, -100)
+    rd = r.cuda()
+    _close("logp[rows]", logp[rd], lp_ref, LOGP_ATOL, 0)
+    assert np.array_equal(m[rd].cpu().double().numpy()[okr], m_ref[okr])
+    _close("log_sum[rows]", ls[rd][torch.as_tensor(okr).cuda()], ls_ref[okr], 1e-4, 0)
+    _close("grad_logits[rows]", grad[rd], lo.backward(gl[r].double().numpy(), zr, tr), *TOL[torch.bfloat16])
+    logp2, m2, ls2 = llp.fused_logp_fwd(zd, td)
+    assert torch.equal(logp, logp2) and torch.equal(m, m2) and torch.equal(ls, ls2)
+    assert torch.equal(grad, llp.fused_logp_bwd(gd, m, ls, zd, td))
