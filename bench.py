@@ -579,6 +579,84 @@ def run_fused(args):
     return 0
 
 
+def run_indexed(args):
+    """Row-subset variant (linear_logp_fwd_indexed / _bwd_indexed) on a seeded
+    subset of round(select_frac * N) rows of the workload, timed against the plain
+    path on the same rows compacted into a K-row problem: the difference is the
+    cost of selecting, compacting and scattering back."""
+    import torch
+
+    from lm_head_selected_gb300 import build
+    build.build()
+    import lm_head_selected_gb300 as llp
+
+    inp, desc = make_workload(args.workload)
+    N, D, V = inp.N, inp.D, inp.V
+    dev = torch.device("cuda", 0)
+    h, w, t, g = inp.hidden.to(dev), inp.weight.to(dev), inp.targets.to(dev), inp.grad_logp.to(dev)
+    b = None if inp.bias is None else inp.bias.to(dev)
+    tau = None if inp.temperature is None else inp.temperature.to(dev)
+    K = max(1, min(N, int(round(args.select_frac * N))))
+    idx = torch.randperm(N, generator=torch.Generator().manual_seed(1006))[:K].sort().values.to(dev)
+    logp = torch.zeros(N, dtype=torch.float32, device=dev)
+    lse = torch.full((N,), float("-inf"), dtype=torch.float32, device=dev)
+
+    def indexed():
+        llp.ops.linear_logp_fwd_indexed(h, w, t, idx, b, tau, out=(logp, lse))
+        llp.ops.linear_logp_bwd_indexed(g, lse, h, w, t, idx, b, tau)
+
+    hk, tk, gk = h[idx].contiguous(), t[idx].contiguous(), g[idx].contiguous()
+    tauk = None if tau is None else tau[idx].contiguous()
+    ws_f = torch.empty(llp.fwd_workspace_bytes(K, D, V), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(llp.bwd_workspace_bytes(K, D, V, b is not None), dtype=torch.uint8, device=dev)
+    lpk = torch.empty(K, dtype=torch.float32, device=dev)
+    lsek = torch.empty(K, dtype=torch.float32, device=dev)
+
+    def plain():
+        llp.linear_logp_fwd(hk, w, tk, b, tauk, workspace=ws_f, out=(lpk, lsek))
+        llp.linear_logp_bwd(gk, lsek, hk, w, tk, b, tauk, workspace=ws_b)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    # alternate the two (A B B A) so that neither gets the cooler, faster clock
+    clocks = ClockSampler(0)
+    clocks.start()
+    i_ms = timed(indexed)
+    p_ms = timed(plain)
+    p_ms = (p_ms + timed(plain)) / 2
+    i_ms = (i_ms + timed(indexed)) / 2
+    clk = clocks.stop()
+    if llp.device_status() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
+    peaks = load_peaks()
+    tflops = 6.0 * K * V * D / (i_ms * 1e-3) / 1e12
+    line = {
+        "metric": "row-subset fwd+bwd selected tokens/s", "value": K / (i_ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": i_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if h.dtype == torch.float16 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}, indexed: {K} of {N} rows", "N": N, "K": K, "D": D, "V": V,
+                   "description": desc},
+        "tensor_peak_frac": tflops / peaks["bf16_tflops_sustained"],
+        "plain_same_rows_ms": p_ms,
+        "selection_overhead": i_ms / p_ms - 1.0,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -590,13 +668,17 @@ def main(argv=None):
     ap.add_argument("--reference-rows", type=int, default=64, help="token rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", choices=("bf16", "fp16"), default="bf16", help="hidden / weight type")
-    ap.add_argument("--op", choices=("linear_logp", "fused_logp"), default="linear_logp",
-                    help="linear_logp: the fused LM-head path (default); fused_logp: the logits-input op")
+    ap.add_argument("--op", choices=("linear_logp", "fused_logp", "indexed"), default="linear_logp",
+                    help="linear_logp: the fused LM-head path (default); fused_logp: the logits-input op; "
+                         "indexed: the row-subset variant on --select-frac of the workload's rows")
+    ap.add_argument("--select-frac", type=float, default=0.5)
     ap.add_argument("--fused-n", type=int, default=16384)
     ap.add_argument("--fused-v", type=int, default=131072)
     args = ap.parse_args(argv)
     if args.op == "fused_logp":
         return run_fused(args)
+    if args.op == "indexed":
+        return run_indexed(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
