@@ -657,6 +657,90 @@ def run_indexed(args):
     return 0
 
 
+def run_shards(args):
+    """Vocab-parallel device work of one rank on one GPU: the workload's head cut
+    into R equal contiguous vocab shards; rank 0's step is its shard forward, the
+    merge of the R gathered (max, sum, target logit) triples, its shard backward
+    and the rank-ordered sum of the R fp32 grad_hidden contributions.  The other
+    ranks' triples and contributions are computed once beforehand, standing in for
+    the all-gathers (not timed: one GPU, no interconnect).  Timed against the
+    unsharded step on the same GPU."""
+    import torch
+
+    from lm_head_selected_gb300 import build, tp
+    build.build()
+    import lm_head_selected_gb300 as llp
+
+    inp, desc = make_workload(args.workload)
+    N, D, V = inp.N, inp.D, inp.V
+    R = args.shards
+    if V % R:
+        raise ValueError("--shards must divide the vocabulary size")
+    Vl = V // R
+    dev = torch.device("cuda", 0)
+    h, w, t, g = inp.hidden.to(dev), inp.weight.to(dev), inp.targets.to(dev), inp.grad_logp.to(dev)
+    b = None if inp.bias is None else inp.bias.to(dev)
+    tau = None if inp.temperature is None else inp.temperature.to(dev)
+    shard = [(w[r * Vl:(r + 1) * Vl], None if b is None else b[r * Vl:(r + 1) * Vl]) for r in range(R)]
+    gathered = torch.stack([tp.fwd_shard(h, ws_, t, r * Vl, bs_, tau) for r, (ws_, bs_) in enumerate(shard)])
+    _, lse0 = tp.merge_shards(gathered, t, V)
+    parts = torch.stack([tp.bwd_shard(g, lse0, h, ws_, t, r * Vl, V, bs_, tau)[0]
+                         for r, (ws_, bs_) in enumerate(shard)])
+
+    def rank0():
+        gathered[0] = tp.fwd_shard(h, shard[0][0], t, 0, shard[0][1], tau)
+        _, lse = tp.merge_shards(gathered, t, V)
+        parts[0] = tp.bwd_shard(g, lse, h, shard[0][0], t, 0, V, shard[0][1], tau)[0]
+        tp.sum_partials(parts, h.dtype)
+
+    ws_f = torch.empty(llp.fwd_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(llp.bwd_workspace_bytes(N, D, V, b is not None), dtype=torch.uint8, device=dev)
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+
+    def whole():
+        llp.linear_logp_fwd(h, w, t, b, tau, workspace=ws_f, out=(logp, lse))
+        llp.linear_logp_bwd(g, lse, h, w, t, b, tau, workspace=ws_b)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    s_ms = timed(rank0)
+    u_ms = timed(whole)
+    u_ms = (u_ms + timed(whole)) / 2
+    s_ms = (s_ms + timed(rank0)) / 2
+    clk = clocks.stop()
+    if llp.device_status() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait")
+    line = {
+        "metric": "vocab-parallel fwd+bwd device time of one rank", "value": s_ms, "unit": "ms",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": s_ms,
+        "higher_is_better": False, "scaling": "strong", "vs_baseline": None,
+        "dtype": "f16" if h.dtype == torch.float16 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}, {R} vocab shards of {Vl}", "N": N, "D": D, "V": V, "shards": R,
+                   "description": desc, "exchange": "not timed (one GPU): the all-gathers of the triples and "
+                                                    "of the fp32 grad_hidden contributions"},
+        "unsharded_ms": u_ms,
+        "rank_share_of_unsharded": s_ms / u_ms,
+        "ideal_share": 1.0 / R,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -668,10 +752,12 @@ def main(argv=None):
     ap.add_argument("--reference-rows", type=int, default=64, help="token rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", choices=("bf16", "fp16"), default="bf16", help="hidden / weight type")
-    ap.add_argument("--op", choices=("linear_logp", "fused_logp", "indexed"), default="linear_logp",
+    ap.add_argument("--op", choices=("linear_logp", "fused_logp", "indexed", "shards"), default="linear_logp",
                     help="linear_logp: the fused LM-head path (default); fused_logp: the logits-input op; "
-                         "indexed: the row-subset variant on --select-frac of the workload's rows")
+                         "indexed: the row-subset variant on --select-frac of the workload's rows; "
+                         "shards: one rank's device work of the vocab-parallel path with --shards shards")
     ap.add_argument("--select-frac", type=float, default=0.5)
+    ap.add_argument("--shards", type=int, default=2)
     ap.add_argument("--fused-n", type=int, default=16384)
     ap.add_argument("--fused-v", type=int, default=131072)
     args = ap.parse_args(argv)
@@ -679,6 +765,8 @@ def main(argv=None):
         return run_fused(args)
     if args.op == "indexed":
         return run_indexed(args)
+    if args.op == "shards":
+        return run_shards(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
