@@ -61,3 +61,13 @@ def test_our_arm_line():
     assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
     clocks = line["clocks"]
     assert "sm_mhz" in clocks and "sm_max_mhz" in clocks and isinstance(clocks["reasons"], list)
+
+
+@pytest.mark.gpu
+def test_row_subset_and_shard_modes_run():
+    """The secondary measurement modes run and report what they time."""
+    line = _run("--op", "indexed", "--workload", "tiny", "--select-frac", "0.25", "--steps", "2", "--warmup", "3")
+    assert line["config"]["K"] == 16 and line["value"] > 0 and line["plain_same_rows_ms"] > 0
+    line = _run("--op", "shards", "--workload", "tiny", "--shards", "2", "--steps", "2", "--warmup", "3")
+    assert line["config"]["shards"] == 2 and line["ms_per_step"] > 0 and line["unsharded_ms"] > 0
+    assert line["higher_is_better"] is False
