@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -68,10 +69,10 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
 # tcgen05 GEMM kernel from one single-pass ncu capture of the default workload,
-# valid only while the kernel sources are unchanged (checked by hash).
+# valid only while the kernel sources are unchanged (checked by sources_sha).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "217cbcc2a155e04e",
+    "sources_sha": "3899ed93af41766f",
     "bytes_per_launch": {"fwd_partials": 2169387264 + 37225728, "dlogits": 6398021376 + 4268878336,
                          "grad_hidden": 24050236672 + 694915840, "grad_weight": 16667673088 + 701035264},
 }
@@ -79,14 +80,20 @@ NCU_TRAFFIC = {
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
 
 
-def sources_sha() -> str:
-    csrc = os.path.join(ROOT, "lm_head_selected_gb300", "csrc")
+def sources_sha(csrc=None) -> str:
+    """Hash of the CUDA / C++ sources with comments and blank space removed, so a
+    comment edit keeps the recorded traffic valid and a code edit does not."""
+    csrc = csrc or os.path.join(ROOT, "lm_head_selected_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                text = fh.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            text = " ".join(text.split())
+            h.update(f.encode())
+            h.update(text.encode())
     return h.hexdigest()[:16]
 
 

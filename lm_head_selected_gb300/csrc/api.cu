@@ -288,8 +288,9 @@ void rec_mark(cudaStream_t s, int id) {
 // Row tiling of the two token-row GEMMs (forward logits, dlogits) for a batch of
 // N rows.  A batch that fits in one 128-row tile runs on single CTAs: in a CTA
 // pair the second CTA's 128 rows would all be padding, and single CTAs put
-// every SM on the weight stream.  Both tilings issue the same tensor-core MMAs
-// along K for every element, so a row's results do not depend on which ran.
+// every SM on the weight stream.  Both tilings accumulate every element over the
+// same 16-deep K steps in the same order (cta_group::1 M=128 or cta_group::2
+// M=256 instructions), and a row's results are bitwise the same under both.
 struct RowTiling {
   bool single;
   int unit_rows;   // rows per unit: kTileM single, kUnitM pair
