@@ -71,3 +71,16 @@ def test_row_subset_and_shard_modes_run():
     line = _run("--op", "shards", "--workload", "tiny", "--shards", "2", "--steps", "2", "--warmup", "3")
     assert line["config"]["shards"] == 2 and line["ms_per_step"] > 0 and line["unsharded_ms"] > 0
     assert line["higher_is_better"] is False
+
+
+def test_sources_hash_ignores_comments_only(tmp_path):
+    """The recorded ncu traffic stays valid across comment edits, never across code edits."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// a kernel\n__global__ void k(int* p) { p[0] = 1; /* store */ }\n")
+    base = bench.sources_sha(str(tmp_path))
+    src.write_text("// the same kernel, reworded\n__global__ void k(int* p) {\n  p[0] = 1;  // one store\n}\n")
+    assert bench.sources_sha(str(tmp_path)) == base
+    src.write_text("// a kernel\n__global__ void k(int* p) { p[0] = 2; /* store */ }\n")
+    assert bench.sources_sha(str(tmp_path)) != base
