@@ -205,3 +205,48 @@ def test_call_from_a_fresh_thread():
     gh, gw, gb = out["g"]
     assert torch.equal(logp, logp0) and torch.equal(lse, lse0)
     assert torch.equal(gh, gh0) and torch.equal(gw, gw0) and torch.equal(gb, gb0)
+
+
+def test_concurrent_threads_on_their_own_streams():
+    """Four host threads, each with its own CUDA stream and its own problem, run
+    forward + backward at the same time; each gets exactly what it gets alone (the
+    entry points share no per-call state)."""
+    import threading
+
+    import lm_head_selected_gb300 as llp
+    shapes = [(300, 256, 5000, 11), (64, 512, 4096, 12), (129, 136, 1000, 13), (32, 2688, 131072, 14)]
+    probs, alone = [], []
+    for N, D, V, seed in shapes:
+        inp = workloads.make_inputs(N, D, V, seed=seed, weight_std=2.0 / math.sqrt(D), bias_std=0.2,
+                                    temperature_range=(0.8, 1.2), n_ignore=2, grad_std=1.0)
+        d = to_device(inp)
+        lp, ls = gpu_fwd(d)
+        alone.append((lp, ls) + tuple(gpu_bwd(d, ls)))
+        probs.append(d)
+    torch.cuda.synchronize()
+    results, errors = [None] * len(probs), []
+    start = threading.Barrier(len(probs))
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                start.wait()
+                for _ in range(3):
+                    lp, ls = gpu_fwd(probs[i])
+                    out = (lp, ls) + tuple(gpu_bwd(probs[i], ls))
+            s.synchronize()
+            results[i] = out
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(probs))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    check_device_status()
+    for got, ref in zip(results, alone):
+        for a, b in zip(got, ref):
+            assert (a is None and b is None) or torch.equal(a, b)
