@@ -128,7 +128,10 @@ int linear_logp_fwd(const void* hidden, const void* weight, const float* bias, c
  *   - No cudaMalloc / cudaFree or any allocating call is made.
  *   - The first call on a device performs a one-time set-up with that device
  *     current (it looks up the array's device address); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address it keeps (like the library's
+ *     other per-device set-up: kernel attributes, the status word) belongs to
+ *     that device's context: after the host program destroys the context
+ *     (cudaDeviceReset), unload and reload the library before calling it again.
  *   - All calls share the one array and it keeps the last call's contents;
  *     nothing in it has to start at zero, because every call writes each
  *     scratch entry it later reads.  Calls whose work overlaps on the GPU

@@ -444,8 +444,10 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     rec_mark(s, kKGradHidden);
     if (p.nseg > 1) {
       const cudaError_t e =
-          p.f32_out ? llp::launch_segment_sum_f32(p.part, p.nseg, static_cast<long long>(N) * D, grad_hidden_f32, s)
-                    : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, s, p.f16);
+          p.f32_out ? llp::launch_segment_sum_f32(p.part, p.nseg, static_cast<long long>(N) * D, grad_hidden_f32,
+                                                  dev->num_sms, s)
+                    : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, dev->num_sms, s,
+                                              p.f16);
       if (e != cudaSuccess) return fail_cuda(__LINE__);
       rec_mark(s, kKSegSumHidden);
     }
@@ -477,7 +479,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       return fail_cuda(__LINE__);
     rec_mark(s, kKGradWeight);
     if (p.nseg > 1) {
-      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, s, p.f16) != cudaSuccess)
+      if (llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(V) * D, p.out, dev->num_sms, s, p.f16) !=
+          cudaSuccess)
         return fail_cuda(__LINE__);
       rec_mark(s, kKSegSumWeight);
     }
@@ -927,7 +930,7 @@ static int sum_partials_entry(const float* parts, int64_t R, int64_t count, void
   const int st = init_device(&dev);
   if (st != LLP_OK) return st;
   return llp::launch_segment_sum(parts, static_cast<int>(R), count, static_cast<__nv_bfloat16*>(out_bf16),
-                                 static_cast<cudaStream_t>(stream), f16 ? 1 : 0) == cudaSuccess
+                                 dev->num_sms, static_cast<cudaStream_t>(stream), f16 ? 1 : 0) == cudaSuccess
              ? LLP_OK : fail_cuda(__LINE__);
 }
 
@@ -1175,39 +1178,9 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   if ((st = load_encode_fn()) != LLP_OK) return st;
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != LLP_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  const RowTiling T = row_tiling(N);
-  CUtensorMap tm_h, tm_w;
-  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM) != LLP_OK) return fail_cuda(__LINE__);
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, T.w_box_rows) != LLP_OK) return fail_cuda(__LINE__);
-
-  uint8_t* ws = static_cast<uint8_t*>(scratch);
-  llp::FwdParams p;
-  p.N = static_cast<int>(N);
-  p.D = static_cast<int>(D);
-  p.V = static_cast<int>(V);
-  p.num_m = static_cast<int>(cdiv(N, T.unit_rows));
-  p.num_vt = static_cast<int>(cdiv(V, llp::kTileN));
-  p.num_splits = static_cast<int>(cdiv(V, llp::kSplitWidth));
-  p.group_m = llp::kGroupM;
-  p.bias = bias;
-  p.targets = reinterpret_cast<const long long*>(targets);
-  p.temperature = temperature;
-  p.ignore_index = ignore_index;
-  p.part_m = reinterpret_cast<float*>(ws + L.part_m);
-  p.part_s = reinterpret_cast<float*>(ws + L.part_s);
-  p.zt = reinterpret_cast<float*>(ws + L.zt);
-  p.err = dev->status_ptr;
-  p.vocab_start = 0;
-  p.global_V = V;
-  p.f16 = 0;
-
-  const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
-  if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s, T.single) != cudaSuccess)
-    return fail_cuda(__LINE__);
-  if (llp::launch_fwd_merge(p, out_logp, out_lse, s) != cudaSuccess) return fail_cuda(__LINE__);
-  return LLP_OK;
+  // the same launch sequence as linear_logp_fwd, with the fixed array as its workspace
+  return fwd_core(dev, hidden, weight, bias, targets, temperature, N, D, V, ignore_index, out_logp, out_lse,
+                  static_cast<uint8_t*>(scratch), static_cast<cudaStream_t>(stream));
 }
 
 int linear_logp_profile_start(int capacity) {

@@ -384,21 +384,26 @@ cudaError_t launch_grad_weight(const CUtensorMap& tm_dz_mn, const CUtensorMap& t
   return launch_units<GradCfg<true, true>>(tm_dz_mn, tm_h_mn, tm_out, p, units, caps.gw_groups, s);
 }
 
-cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s,
-                               int f16) {
-  const int threads = 256;
+// Grid-stride kernels: enough blocks to fill the device (16 per SM), never more than the work.
+static long long segment_sum_blocks(long long count, int threads, int num_sms) {
   long long blocks = (count / 4 + threads - 1) / threads;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
-  if (blocks < 1) blocks = 1;
+  const long long cap = 16LL * (num_sms > 0 ? num_sms : 1);
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : blocks;
+}
+
+cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, int num_sms,
+                               cudaStream_t s, int f16) {
+  const int threads = 256;
+  const long long blocks = segment_sum_blocks(count, threads, num_sms);
   segment_sum_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out, f16);
   return launch_result();
 }
 
-cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, cudaStream_t s) {
+cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, int num_sms,
+                                   cudaStream_t s) {
   const int threads = 256;
-  long long blocks = (count / 4 + threads - 1) / threads;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
-  if (blocks < 1) blocks = 1;
+  const long long blocks = segment_sum_blocks(count, threads, num_sms);
   segment_sum_f32_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
   return launch_result();
 }

@@ -131,7 +131,9 @@ cudaError_t launch_shard_stats(const FwdParams& p, float* out_max, float* out_su
 cudaError_t launch_merge_shards(const float* mx, const float* se, const float* tl, int R, int N,
                                 const long long* targets, long long global_V, long long ignore_index, float* out_logp,
                                 float* out_lse, cudaStream_t s);
-cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, cudaStream_t s);
+// num_sms: the device's SM count (the grid is at most 16 blocks per SM).
+cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count, float* out, int num_sms,
+                                   cudaStream_t s);
 
 cudaError_t bwd_setup(LaunchCaps* caps);
 // The third tensor map is the output the epilogue stores through: dz (bf16,
@@ -183,9 +185,10 @@ cudaError_t scatter_selected_outputs(const RowSelection& sel, const float* c_log
 cudaError_t scatter_selected_grad_hidden(const RowSelection& sel, int N, int D, const __nv_bfloat16* c_gh,
                                          __nv_bfloat16* gh, cudaStream_t s);
 
-// out: bf16, or fp16 when f16 != 0
-cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, cudaStream_t s,
-                               int f16 = 0);
+// out: bf16, or fp16 when f16 != 0; num_sms: the device's SM count (the grid
+// is at most 16 blocks per SM).
+cudaError_t launch_segment_sum(const float* part, int nseg, long long count, __nv_bfloat16* out, int num_sms,
+                               cudaStream_t s, int f16 = 0);
 cudaError_t launch_bias_sum(const float* gb_part, int nblocks, int V, float* out, cudaStream_t s);
 
 }  // namespace llp

@@ -5,12 +5,21 @@ weight shard [V_local, D] (and bias shard) starting at global vocab id
 ``vocab_start``; the shards partition [0, global_vocab_size).  Each rank
 computes its shard's per-row (max, sum of exp, target logit); the ranks
 all-gather these triples and merge them in ascending rank order; in the
-backward every rank forms its local dlogits with the merged lse, the fp32
-grad_hidden contributions are all-gathered and summed in ascending rank order
-(rounded once to bf16), and the weight / bias gradients stay local.  Merging
-gathered values in rank order (instead of an all-reduce whose summation order
-belongs to the collective library) keeps the result independent of collective
-timing.
+backward every rank forms its local dlogits with the merged lse, and the fp32
+grad_hidden contributions are summed over ranks in ascending rank order and
+rounded once to bf16 (the page's all-reduce of hidden.grad); the weight / bias
+gradients stay local.  Summing in a fixed rank order (instead of an all-reduce
+whose summation order belongs to the collective library) keeps the result
+independent of collective timing.
+
+The grad_hidden sum is a reduce-scatter done by hand: an all_to_all hands rank
+q every rank's contribution to the q-th block of token rows, rank q sums its
+block in ascending rank order and rounds it once, and an all_gather of the
+rounded blocks gives every rank the whole gradient.  Per rank that moves
+(R-1)/R * N*D*(4 + 2) bytes, against (R-1) * N*D*4 bytes (and an R*N*D*4-byte
+buffer) for all-gathering every contribution; each element's sum has the same
+terms in the same order either way, so both give the same bits
+(``grad_hidden_exchange="gather"`` keeps the gather form).
 
 The device work is in ``liblinear_logp.so``; torch.distributed moves the
 triples and partials.  ``ShardOps`` groups the device operations; the default
@@ -113,41 +122,74 @@ def _all_gather(t: torch.Tensor, group) -> torch.Tensor:
     return torch.stack(outs)
 
 
+def rank_ordered_sum(part: torch.Tensor, group, dtype, ops: "ShardOps",
+                     exchange: str = "reduce_scatter") -> torch.Tensor:
+    """Sum over the ranks of ``group`` of each rank's fp32 ``part`` [N, D], in
+    ascending rank order, rounded once to ``dtype``; the whole result on every rank.
+
+    exchange="reduce_scatter": all_to_all of row blocks of ceil(N/R) rows (the
+    last block zero-padded), an ordered sum of this rank's block, all_gather of
+    the rounded blocks.  exchange="gather": all_gather of every rank's whole
+    contribution, then the ordered sum of all of it.  Same terms, same order,
+    same rounding per element: the same bits.
+    """
+    if exchange == "gather":
+        return ops.sum_partials(_all_gather(part, group), dtype)
+    if exchange != "reduce_scatter":
+        raise ValueError(f"unknown grad_hidden exchange {exchange!r}")
+    world = dist.get_world_size(group)
+    N, D = part.shape
+    rows = -(-N // world) if N else 0
+    send = part.contiguous()
+    if rows * world != N:
+        send = torch.cat([send, send.new_zeros((rows * world - N, D))])
+    recv = torch.empty_like(send)  # block r: rank r's contribution to this rank's rows
+    dist.all_to_all_single(recv, send, group=group)
+    mine = ops.sum_partials(recv.view(world, rows, D), dtype)
+    out = mine.new_empty((world * rows, D))
+    dist.all_gather_into_tensor(out, mine.contiguous(), group=group)
+    return out[:N]
+
+
 class _VocabParallelLinearLogp(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight_local, bias_local, targets, temperature, group, vocab_start, global_v,
-                ignore_index, ops):
+                ignore_index, ops, exchange):
         stats = ops.fwd_shard(hidden, weight_local, targets, vocab_start, bias_local, temperature, ignore_index)
         gathered = _all_gather(stats, group)
         logp, lse = ops.merge_shards(gathered, targets, global_v, ignore_index)
         ctx.save_for_backward(hidden, weight_local, bias_local, targets, temperature, lse)
-        ctx.meta = (group, vocab_start, global_v, ignore_index, ops)
+        ctx.meta = (group, vocab_start, global_v, ignore_index, ops, exchange)
         return logp
 
     @staticmethod
     def backward(ctx, grad_logp):
         hidden, weight_local, bias_local, targets, temperature, lse = ctx.saved_tensors
-        group, vocab_start, global_v, ignore_index, ops = ctx.meta
+        group, vocab_start, global_v, ignore_index, ops, exchange = ctx.meta
         gh_part, gw, gb = ops.bwd_shard(grad_logp.contiguous().float(), lse, hidden, weight_local, targets,
                                         vocab_start, global_v, bias_local, temperature, ignore_index,
                                         ctx.needs_input_grad[1], ctx.needs_input_grad[2])
-        gh = ops.sum_partials(_all_gather(gh_part, group), hidden.dtype) if ctx.needs_input_grad[0] else None
-        return gh, gw, gb, None, None, None, None, None, None, None
+        gh = rank_ordered_sum(gh_part, group, hidden.dtype, ops, exchange) if ctx.needs_input_grad[0] else None
+        return gh, gw, gb, None, None, None, None, None, None, None, None
 
 
 def linear_logp_vocab_parallel(hidden: torch.Tensor, weight_local: torch.Tensor, targets: torch.Tensor,
                                bias_local: Optional[torch.Tensor] = None,
                                temperature: Optional[torch.Tensor] = None, *, group=None, vocab_start: int,
                                global_vocab_size: int, ignore_index: int = IGNORE_INDEX,
-                               ops: Optional[ShardOps] = None) -> torch.Tensor:
+                               ops: Optional[ShardOps] = None,
+                               grad_hidden_exchange: str = "reduce_scatter") -> torch.Tensor:
     """Per-token log-prob with the LM head sharded over the vocab across ``group``.
 
     hidden [N, D] (replicated), weight_local [V_local, D] rows vocab_start ..
     vocab_start + V_local - 1 of the global head, targets [N] global ids
     (replicated), bias_local [V_local] optional.  Returns logp fp32 [N]; its
-    backward gives grad_hidden (summed over ranks) and the local weight / bias
+    backward gives grad_hidden (summed over ranks in ascending rank order; see
+    ``rank_ordered_sum`` for the two exchanges) and the local weight / bias
     gradients.
     """
+    if grad_hidden_exchange not in ("reduce_scatter", "gather"):
+        raise ValueError(f"unknown grad_hidden exchange {grad_hidden_exchange!r}")
     return _VocabParallelLinearLogp.apply(hidden, weight_local, bias_local, targets, temperature, group,
                                           int(vocab_start), int(global_vocab_size), int(ignore_index),
-                                          ops or ShardOps())
+                                          ops or ShardOps(), grad_hidden_exchange)

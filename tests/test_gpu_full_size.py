@@ -1,7 +1,9 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark
 times: every forward row checked for validity, sampled rows against the FP64
-oracle, grad_weight checked in full on a batch whose active rows the oracle
-can afford (all other rows ignored, so the full-size GEMMs still run over
+oracle, grad_weight / grad_bias of the dense batch itself on sampled vocab rows
+(every token contributes; the oracle needs every row's log-sum-exp for that, one
+FP64 pass over the logits), grad_weight in full on a batch whose active rows the
+oracle can afford (all other rows ignored, so the full-size GEMMs still run over
 every token), and bitwise repeatability."""
 import numpy as np
 import pytest
@@ -58,6 +60,36 @@ def _zero_sum_identities(inp, gw, gb=None):
         assert abs(float(gb.double().sum())) <= 1e-4 * float(gs.sum())
 
 
+def _vocab_rows(inp, k, seed, tile_edges=()):
+    """About k vocab rows for a sampled grad_weight check: the targets of several
+    valid token rows (their one-hot term lands there), the first and last rows,
+    both sides of the given 256-row tile / 128-row CTA edges, and seeded random rows."""
+    t = inp.targets
+    valid = oracle.valid_rows(t.numpy(), inp.V, inp.ignore_index)
+    hit = [int(x) for x in t[torch.as_tensor(valid)][:8].tolist()]
+    fixed = {0, 1, inp.V - 1, *hit}
+    for e in tile_edges:
+        fixed |= {e - 1, e}
+    g = torch.Generator().manual_seed(seed)
+    rnd = torch.randperm(inp.V, generator=g)[: max(0, k - len(fixed))].tolist()
+    return sorted(v for v in fixed | set(rnd) if 0 <= v < inp.V)
+
+
+def _check_dense_grad_weight_rows(inp, gw, gb, vrows):
+    """grad_weight[vrows] (and grad_bias[vrows]) of the dense batch against the
+    oracle's sampled-row form, element by element at the reduction tolerance
+    ("Feat/nemotron h lm head logprob cuda", Tolerance: atol 0.1 / rtol 0.02)."""
+    a = oracle_args(inp)
+    gw_ref, gb_ref = oracle.grad_weight_rows(np64(inp.grad_logp), a[0], a[1], a[2], a[3], a[4], vrows,
+                                             ignore_index=inp.ignore_index)
+    idx = torch.as_tensor(vrows, device=gw.device)
+    assert_close("grad_weight[vocab rows]", np64(gw[idx]), gw_ref, GW_ATOL, GW_RTOL)
+    if gb is not None:
+        assert_close("grad_bias[vocab rows]", np64(gb[idx]), gb_ref, GW_ATOL, GW_RTOL)
+    # the check is not vacuous: the sampled rows carry gradients well above the tolerance's floor
+    assert float(np.abs(gw_ref).max()) > 2 * GW_ATOL
+
+
 def _sparse_targets(inp, active, seed):
     """Same inputs, but only `active` rows keep their target; the rest are ignored."""
     g = torch.Generator().manual_seed(seed)
@@ -87,7 +119,8 @@ def test_rl_scoring_forward_full_size():
 
 def test_rl_head_fwd_bwd_full_size():
     """The benchmark's step (N=16384, D=2688, V=131072, grad_logp ~ N(0,1)): sampled
-    grad_hidden rows, full grad_weight on a batch with 192 active rows."""
+    grad_hidden rows, sampled grad_weight rows of the dense batch, full grad_weight
+    on a batch with 192 active rows."""
     inp = workloads.rl_scoring(seed=1002, grad_std=1.0)
     d = to_device(inp)
     logp, lse = gpu_fwd(d)
@@ -98,6 +131,7 @@ def test_rl_head_fwd_bwd_full_size():
     gh2, gw2, _ = gpu_bwd(d, lse)
     assert torch.equal(gh, gh2) and torch.equal(gw, gw2)
     _zero_sum_identities(inp, gw)
+    _check_dense_grad_weight_rows(inp, gw, None, _vocab_rows(inp, 64, 8, tile_edges=(128, 256, 65536)))
     del gw, gw2, gh2
     sp = _sparse_targets(inp, 192, 3)
     ds = to_device(sp)
@@ -109,7 +143,8 @@ def test_rl_head_fwd_bwd_full_size():
 
 def test_train_step_full_size():
     """N=16384, D=4096, V=128256 with bias: sampled rows of logp / grad_hidden,
-    grad_weight / grad_bias in full on a batch with 128 active rows."""
+    sampled grad_weight / grad_bias rows of the dense batch (including the last
+    256-row vocab tile), grad_weight / grad_bias in full on a batch with 128 active rows."""
     inp = workloads.train()
     d = to_device(inp)
     logp, lse = gpu_fwd(d)
@@ -121,6 +156,7 @@ def test_train_step_full_size():
     check_backward(inp, gh, None, None, rows=rows)
     assert torch.all(torch.isfinite(gb))
     _zero_sum_identities(inp, gw, gb)
+    _check_dense_grad_weight_rows(inp, gw, gb, _vocab_rows(inp, 64, 9, tile_edges=(128, 256, 128000, 128128)))
     del gw, gh
     sp = _sparse_targets(inp, 128, 5)
     ds = to_device(sp)

@@ -1,11 +1,14 @@
 """Vocab-parallel orchestration across ranks, on CPU with gloo (world size 2 and 3).
 
 ``lm_head_selected_gb300.tp.linear_logp_vocab_parallel`` all-gathers the shard
-triples and grad_hidden contributions and merges them in rank order; the
-device work is injected here as small float64 CPU functions of the same
-contract (a shard's max / sum of exp / target logit; the rank-ordered merge;
-the shard's dlogits contractions), so the collective logic, the rank order and
-the autograd wiring are checked without a GPU, against the unsharded oracle."""
+triples and merges them in rank order, and sums the grad_hidden contributions
+in rank order, either by a hand-made reduce-scatter (all_to_all of row blocks,
+ordered sum, all_gather) or by all-gathering every contribution; the device
+work is injected here as small float64 CPU functions of the same contract (a
+shard's max / sum of exp / target logit; the rank-ordered merge; the shard's
+dlogits contractions), so the collective logic, the rank order and the
+autograd wiring are checked without a GPU, against the unsharded oracle, and
+the two grad_hidden exchanges are checked to give the same bits."""
 import math
 import os
 import socket
@@ -88,13 +91,17 @@ def _worker(rank, world, port, q):
     V = inp.V
     cuts = [0, 30, 61, 97] if world == 3 else [0, 45, 97]
     s, e = cuts[rank], cuts[rank + 1]
-    h = inp.hidden.double().requires_grad_(True)
-    w = inp.weight.double()[s:e].clone().requires_grad_(True)
-    b = inp.bias.double()[s:e].clone().requires_grad_(True)
     tau = inp.temperature.double()
-    logp = linear_logp_vocab_parallel(h, w, inp.targets, b, tau, vocab_start=s, global_vocab_size=V,
-                                      ops=_cpu_ops())
-    (logp * inp.grad_logp.double()).sum().backward()
+    grads = {}
+    for exchange in ("reduce_scatter", "gather"):
+        h = inp.hidden.double().requires_grad_(True)
+        w = inp.weight.double()[s:e].clone().requires_grad_(True)
+        b = inp.bias.double()[s:e].clone().requires_grad_(True)
+        logp = linear_logp_vocab_parallel(h, w, inp.targets, b, tau, vocab_start=s, global_vocab_size=V,
+                                          ops=_cpu_ops(), grad_hidden_exchange=exchange)
+        (logp * inp.grad_logp.double()).sum().backward()
+        grads[exchange] = (logp.detach(), h.grad, w.grad, b.grad)
+    same = all(torch.equal(x, y) for x, y in zip(grads["reduce_scatter"], grads["gather"]))
     a = (inp.hidden.double().numpy(), inp.weight.double().numpy(), inp.bias.double().numpy(), inp.targets.numpy(),
          inp.temperature.double().numpy(), -100)
     lp_ref, _ = oracle.forward(*a)
@@ -102,7 +109,7 @@ def _worker(rank, world, port, q):
     err = max(np.abs(logp.detach().numpy() - lp_ref).max(), np.abs(h.grad.numpy() - gh_ref).max(),
               np.abs(w.grad.numpy() - gw_ref[s:e]).max(), np.abs(b.grad.numpy() - gb_ref[s:e]).max())
     dist.destroy_process_group()
-    q.put((rank, float(err)))
+    q.put((rank, float(err), same))
 
 
 @pytest.mark.parametrize("world", [2, 3])
@@ -117,5 +124,48 @@ def test_vocab_parallel_orchestration_gloo(world):
         p.join(timeout=180)
         assert p.exitcode == 0
     res = sorted(q.get(timeout=10) for _ in range(world))
-    assert [r for r, _ in res] == list(range(world))
-    assert all(err < 1e-10 for _, err in res), res
+    assert [r for r, _, _ in res] == list(range(world))
+    assert all(err < 1e-10 for _, err, _ in res), res
+    # the reduce-scatter and the all-gather exchange give bitwise the same gradients
+    assert all(same for _, _, same in res), res
+
+
+def _sum_worker(rank, world, port, q):
+    """rank_ordered_sum on fp32 contributions with the device path's rounding
+    (fp32 sum in ascending rank order, one rounding to bf16), N not a multiple of
+    the world size: both exchanges and a local recomputation agree bitwise."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from lm_head_selected_gb300.tp import ShardOps, rank_ordered_sum
+
+    def sum_partials(parts, dtype):
+        acc = parts[0].clone()
+        for r in range(1, parts.shape[0]):
+            acc = acc + parts[r]
+        return acc.to(dtype)
+
+    ops = ShardOps(sum_partials=sum_partials)
+    N, D = 41, 24
+    every = [torch.randn(N, D, generator=torch.Generator().manual_seed(50 + r)) * (10.0 ** r) for r in range(world)]
+    out_rs = rank_ordered_sum(every[rank], None, torch.bfloat16, ops, "reduce_scatter")
+    out_g = rank_ordered_sum(every[rank], None, torch.bfloat16, ops, "gather")
+    local = sum_partials(torch.stack(every), torch.bfloat16)
+    ok = (out_rs.dtype == torch.bfloat16 and out_rs.shape == (N, D) and torch.equal(out_rs, out_g)
+          and torch.equal(out_rs, local))
+    dist.destroy_process_group()
+    q.put((rank, ok))
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_rank_ordered_sum_exchanges_agree_gloo(world):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_sum_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(world))
+    assert res == [(r, True) for r in range(world)], res

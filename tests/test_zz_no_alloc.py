@@ -4,10 +4,12 @@ It is meant for callers that cannot allocate device memory themselves, such as
 a plugin inside a host program that owns every byte of device memory, or a
 loop where cudaMalloc is not allowed.  Its scratch is a fixed 16 MiB array
 inside the library, shared by every call.  These tests call it through the C
-ABI and check that two calls in a row agree with the regular forward (which
-takes a caller workspace), that a problem too large for the array is refused
-before anything runs, and that the array's leftover contents from a previous
-call do not leak into the next one.
+ABI and check that two calls in a row give bitwise the results of the regular
+forward (which takes a caller workspace: the same kernels with the same
+parameters, so nothing may differ), that sampled rows match the FP64 oracle,
+that a problem too large for the array is refused before anything runs, and
+that the array's leftover contents from a previous call do not leak into the
+next one.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it passes alone in a fresh process too.
@@ -15,12 +17,11 @@ already run every other test; it passes alone in a fresh process too.
 import ctypes
 import math
 
-import numpy as np
 import pytest
 import torch
 
 import workloads
-from parity_helpers import LOGP_ATOL, LSE_ATOL, check_device_status, to_device
+from parity_helpers import check_device_status, check_forward, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -49,15 +50,6 @@ def _regular(d):
                                d["ignore_index"])
 
 
-def _agree(a, b, atol):
-    a = a.double().cpu().numpy()
-    b = b.double().cpu().numpy()
-    assert np.array_equal(np.isfinite(a), np.isfinite(b))
-    fin = np.isfinite(b)
-    assert np.all(np.abs(a[fin] - b[fin]) <= atol)
-    assert np.array_equal(a[~fin], b[~fin])
-
-
 CASES = [
     # (N, D, V, bias, temperature): the Nemotron head near the scratch limit, then a
     # smaller ragged problem, so the second call runs on the first call's leftovers.
@@ -76,8 +68,16 @@ def test_two_calls_in_a_row_match_the_workspace_forward(lib):
         assert st == 0, lib.linear_logp_status_string(st)
         ref_logp, ref_lse = _regular(d)
         check_device_status()
-        _agree(logp, ref_logp, LOGP_ATOL)
-        _agree(lse, ref_lse, LSE_ATOL)
+        # same kernels, same tiling, same fixed-order merge: bitwise equal, the
+        # 0 / -inf of invalid rows included
+        assert torch.equal(logp, ref_logp)
+        assert torch.equal(lse, ref_lse)
+        # and right, not merely consistent: sampled rows (ignored and out-of-range
+        # ones among them) against the FP64 oracle
+        bad = [int(r) for r in torch.nonzero(~torch.isfinite(ref_lse)).flatten()[:4].cpu()]
+        g = torch.Generator().manual_seed(700 + i)
+        rows = sorted(set(torch.randperm(N, generator=g)[:24].tolist()) | {0, N - 1} | set(bad))
+        check_forward(inp, logp, lse, rows=rows)
 
 
 def test_refuses_problems_beyond_the_scratch_limit(lib):
