@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "liblinear_logp.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "logits.cu", "indexed.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "gh_small.cu", "logits.cu", "indexed.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
                 "-I", INCLUDE, "-I", CSRC]

@@ -110,6 +110,7 @@ int init_device(DeviceInit** out) {
     if (major != 10 || minor != 3) {
       d.status = LLP_ERR_UNSUPPORTED_DEVICE;
     } else if (llp::fwd_setup(&d.caps) != cudaSuccess || llp::bwd_setup(&d.caps) != cudaSuccess ||
+               llp::small_grad_hidden_setup() != cudaSuccess ||
                cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_ptr), g_status_word) != cudaSuccess) {
       d.status = fail_cuda(__LINE__);
     } else {
@@ -216,6 +217,25 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
                               const_cast<void*>(base), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
+  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
+}
+
+// 3-D map of a row-major 16-bit matrix [rows][cols] (row pitch pitch_bytes) seen
+// as its 64-column chunks: {64, rows, cols / 64} with strides {pitch, 128 B}.  A
+// box {64, box_rows, box_chunks} lands in shared memory as box_chunks 2-D
+// {64, box_rows} boxes back to back.  cols must be a multiple of 64 (chunks never
+// straddle a row end).
+int make_map_chunked(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_bytes,
+                     uint32_t box_rows, uint32_t box_chunks, bool f16) {
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {pitch_bytes, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
   return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
 }
@@ -355,6 +375,17 @@ bool force_static_schedule() {
   return v;
 }
 
+// LINEAR_LOGP_SMALL_GRAD_HIDDEN=0 (read once per process) sends batches of at
+// most kSmallGhMaxN rows through the CTA-pair grad_hidden GEMM instead of the
+// swapped-operand kernel.  A diagnostic: both give the same results.
+bool use_small_grad_hidden() {
+  static const bool v = [] {
+    const char* e = std::getenv("LINEAR_LOGP_SMALL_GRAD_HIDDEN");
+    return LLP_SMALL_GH != 0 && !(e != nullptr && std::strcmp(e, "0") == 0);
+  }();
+  return v;
+}
+
 // K-blocks of a gradient GEMM's longest unit (a full K segment, or all of K
 // when it is shorter).  The long units carry the work and the L2 reuse that
 // in-order claiming protects; a short last segment rides along.
@@ -409,8 +440,10 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.f16 = f16 ? 1 : 0;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
-    CUtensorMap tm_dz_out;  // dz [N][V] (row pitch V_pad), written in 64 x 32 slabs
-    if (make_map(&tm_dz_out, dz, V, N, V_pad * 2, 64, 32, f16) != LLP_OK) return fail_cuda(__LINE__);
+    // dz [N][V_pad], written in 64 x 32 slabs; the columns [V, V_pad) of the last
+    // slab are zeros, so readers may treat every row as V_pad long
+    CUtensorMap tm_dz_out;
+    if (make_map(&tm_dz_out, dz, V_pad, N, V_pad * 2, 64, 32, f16) != LLP_OK) return fail_cuda(__LINE__);
     if (llp::launch_dlogits(tm_h, tm_w, tm_dz_out, p, units, dev->caps, s, T.single) != cudaSuccess)
       return fail_cuda(__LINE__);
     rec_mark(s, kKDlogits);
@@ -418,36 +451,66 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
 
   // B2: grad_hidden = dz . W over fixed vocab segments
   if (want_gh) {
-    CUtensorMap tm_dz, tm_w_mn;
-    if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
-    if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
-    llp::GradGemmParams p;
-    p.rows = static_cast<int>(N);
-    p.D = static_cast<int>(D);
-    p.K = static_cast<int>(V);
-    p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
-    p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
-    p.nseg = static_cast<int>(cdiv(V, llp::kKSegment));
-    p.kseg_blocks = llp::kKSegment / llp::kTileK;
-    p.out = static_cast<__nv_bfloat16*>(grad_hidden);
-    p.part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
-    p.err = dev->status_ptr;
-    p.f32_out = grad_hidden_f32 != nullptr ? 1 : 0;
-    p.f16 = f16 ? 1 : 0;
-    p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
-    if (p.f32_out && p.nseg == 1) p.part = grad_hidden_f32;  // one segment: write the fp32 result directly
-    const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
-    CUtensorMap tm_out;
-    if (make_map_grad_out(&tm_out, p) != LLP_OK) return fail_cuda(__LINE__);
-    if (llp::launch_grad_hidden(tm_dz, tm_w_mn, tm_out, p, units, dev->caps, s) != cudaSuccess)
-      return fail_cuda(__LINE__);
+    const int nseg = static_cast<int>(cdiv(V, llp::kKSegment));
+    const bool f32_out = grad_hidden_f32 != nullptr;
+    // fp32 segment partials, or (one segment) a shard's fp32 contribution written directly
+    float* part = L.has_dh ? reinterpret_cast<float*>(ws + L.dh_part) : (f32_out ? grad_hidden_f32 : nullptr);
+    llp::GhSmallParams sp;
+    if (use_small_grad_hidden() && llp::small_grad_hidden_plan(static_cast<int>(N), &sp)) {
+      // a batch of at most kSmallGhMaxN rows: tokens on the MMA's N side, weight streamed in tall boxes
+      CUtensorMap tm_w_rows, tm_dz_tok;
+      sp.w_chunked = (D % 128) == 0 ? 1 : 0;
+      if (sp.w_chunked) {
+        if (make_map_chunked(&tm_w_rows, weight, D, V, D * 2, llp::kSmallGhRows, 2, f16) != LLP_OK)
+          return fail_cuda(__LINE__);
+      } else if (make_map(&tm_w_rows, weight, D, V, D * 2, 64, llp::kSmallGhRows, f16) != LLP_OK) {
+        return fail_cuda(__LINE__);
+      }
+      // dz's padding columns [V, V_pad) are zero (written by the dlogits kernel)
+      if (make_map_chunked(&tm_dz_tok, dz, V_pad, N, V_pad * 2, sp.BN, llp::kSmallGhRows / 64 * sp.b_span, f16) !=
+          LLP_OK)
+        return fail_cuda(__LINE__);
+      sp.D = static_cast<int>(D);
+      sp.V = static_cast<int>(V);
+      sp.nseg = nseg;
+      sp.num_dt = static_cast<int>(cdiv(D, 128));
+      sp.part = part;
+      sp.out = static_cast<__nv_bfloat16*>(grad_hidden);
+      sp.f16 = f16 ? 1 : 0;
+      sp.err = dev->status_ptr;
+      if (llp::launch_small_grad_hidden(tm_w_rows, tm_dz_tok, sp, dev->num_sms, s) != cudaSuccess)
+        return fail_cuda(__LINE__);
+    } else {
+      CUtensorMap tm_dz, tm_w_mn;
+      if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
+      if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
+      llp::GradGemmParams p;
+      p.rows = static_cast<int>(N);
+      p.D = static_cast<int>(D);
+      p.K = static_cast<int>(V);
+      p.num_m = static_cast<int>(cdiv(N, llp::kUnitM));
+      p.num_d = static_cast<int>(cdiv(D, llp::kTileN));
+      p.nseg = nseg;
+      p.kseg_blocks = llp::kKSegment / llp::kTileK;
+      p.out = static_cast<__nv_bfloat16*>(grad_hidden);
+      p.part = part;
+      p.err = dev->status_ptr;
+      p.f32_out = f32_out ? 1 : 0;
+      p.f16 = f16 ? 1 : 0;
+      p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
+      const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
+      CUtensorMap tm_out;
+      if (make_map_grad_out(&tm_out, p) != LLP_OK) return fail_cuda(__LINE__);
+      if (llp::launch_grad_hidden(tm_dz, tm_w_mn, tm_out, p, units, dev->caps, s) != cudaSuccess)
+        return fail_cuda(__LINE__);
+    }
     rec_mark(s, kKGradHidden);
-    if (p.nseg > 1) {
+    if (nseg > 1) {
       const cudaError_t e =
-          p.f32_out ? llp::launch_segment_sum_f32(p.part, p.nseg, static_cast<long long>(N) * D, grad_hidden_f32,
-                                                  dev->num_sms, s)
-                    : llp::launch_segment_sum(p.part, p.nseg, static_cast<long long>(N) * D, p.out, dev->num_sms, s,
-                                              p.f16);
+          f32_out ? llp::launch_segment_sum_f32(part, nseg, static_cast<long long>(N) * D, grad_hidden_f32,
+                                                dev->num_sms, s)
+                  : llp::launch_segment_sum(part, nseg, static_cast<long long>(N) * D,
+                                            static_cast<__nv_bfloat16*>(grad_hidden), dev->num_sms, s, f16 ? 1 : 0);
       if (e != cudaSuccess) return fail_cuda(__LINE__);
       rec_mark(s, kKSegSumHidden);
     }

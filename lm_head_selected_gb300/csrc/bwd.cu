@@ -191,8 +191,13 @@ struct DzCfg {
       // rows >= N and columns >= V are clipped by the store's tensor map; a slab
       // that starts past the last row is not stored at all (warp-uniform)
       if (row0 < p.N) {
-        if (LLP_DZ_STREAM)
-          epi_slab_store_2d_stream(es, sbuf, v0 + 64 * q, row0);
+        // a large batch's dz (GBs) streams through L2 once per gradient GEMM; a
+        // batch of at most 128 rows (single CTAs) has a few MB of dz, which the
+        // grad_hidden kernel right after re-reads for every hidden tile: keep it
+        if (!PAIR)
+          epi_slab_store_2d_hint(es, sbuf, v0 + 64 * q, row0, l2_policy_evict_last());
+        else if (LLP_DZ_STREAM)
+          epi_slab_store_2d_hint(es, sbuf, v0 + 64 * q, row0, l2_policy_evict_first());
         else
           epi_slab_store_2d(es, sbuf, v0 + 64 * q, row0);
       }

@@ -152,14 +152,16 @@ __device__ __forceinline__ void epi_slab_store_2d(EpiStore& es, uint32_t buf, in
   es.next ^= 1u;
 }
 
-// As epi_slab_store_2d, for an output that is streamed once through L2 (the
-// bf16 dlogits): stored with evict-first priority so it does not push out the
-// operand tiles that the running units still re-read.
-__device__ __forceinline__ void epi_slab_store_2d_stream(EpiStore& es, uint32_t buf, int x, int y) {
+// As epi_slab_store_2d, with an L2 eviction-priority hint (a createpolicy
+// value): evict-first for an output that is streamed once through L2 (the bf16
+// dlogits of a large batch), so it does not push out the operand tiles that the
+// running units still re-read; evict-last for one that the next kernel re-reads
+// from L2 (the dlogits of a small batch).
+__device__ __forceinline__ void epi_slab_store_2d_hint(EpiStore& es, uint32_t buf, int x, int y, uint64_t policy) {
   fence_proxy_async_smem();
   __syncwarp();
   if (es.lane == 0) {
-    tma_store_2d_hint(es.map, buf, x, y, l2_policy_evict_first());
+    tma_store_2d_hint(es.map, buf, x, y, policy);
     bulk_commit_group();
   }
   es.next ^= 1u;

@@ -47,6 +47,39 @@ constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 #define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
 #endif
 
+#ifndef LLP_SMALL_GH
+#define LLP_SMALL_GH 1       // grad_hidden of batches of at most kSmallGhMaxN rows on the swapped-operand kernel
+#endif
+
+// grad_hidden of small batches with the hidden dimension on the MMA's M side
+// and the tokens on its N side (gh_small.cu).
+constexpr int kSmallGhMaxN = 128;        // largest batch it takes (tokens padded to a multiple of 16)
+constexpr int kSmallGhRows = 256;        // vocab rows per weight stage (height of the weight boxes)
+constexpr int kSmallGhMaxStages = 8;     // deepest ring of either operand
+constexpr int kSmallGhSmemLimit = 232448;  // dynamic shared memory the kernel may use
+
+struct GhSmallParams {
+  int N, D, V;
+  int BN;            // MMA N: N rounded up to 16
+  int nseg, num_dt;  // vocab segments of kKSegment rows; 128-column hidden tiles
+  int b_span;        // weight stages of kSmallGhRows vocab rows per dz slot
+  int stages_a, stages_b, b_slot_bytes;  // ring depths (weight, dz) and bytes of one dz slot
+  int w_chunked;     // the weight map is 3-D {64, V, D/64}: one copy per stage (D % 128 == 0), else 2-D
+  float* part;          // fp32 [nseg][N][D] (segment partials, or a shard's contribution); nullptr: `out`
+  __nv_bfloat16* out;   // [N][D] bf16 (fp16 when f16), with one segment and part == nullptr
+  int f16;
+  unsigned int* err;
+};
+// Fills N, BN, the ring depths and slot size; false when the batch is too large for the kernel.
+bool small_grad_hidden_plan(int N, GhSmallParams* p);
+cudaError_t small_grad_hidden_setup();
+// tm_w: the weight [V][D] as 64-column chunks, {64, V, D/64} with box {64, kSmallGhRows, 2}
+// (w_chunked), else 2-D {D, V} with box {64, kSmallGhRows}; tm_dz: dz [N][V_pad] as 64-column
+// chunks, {64, N, V_pad/64} with box {64, BN, kSmallGhRows/64 * b_span} (its padding columns
+// must be zero).
+cudaError_t launch_small_grad_hidden(const CUtensorMap& tm_w, const CUtensorMap& tm_dz, const GhSmallParams& p,
+                                     int num_sms, cudaStream_t s);
+
 // Resident work groups (CTA pairs, or CTAs in single mode) per GEMM kernel,
 // found once per device; the persistent grids never exceed them.
 struct LaunchCaps {
