@@ -312,6 +312,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
             : make_smem_desc_sw128(base + kk * (UMMA_K * 2), 16, 1024);
 }
 
+// How far operand_desc's start-address field moves per 16-deep step (16-byte units).
+template <bool MN>
+__device__ __forceinline__ constexpr int operand_step() {
+  return MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+}
+
 template <class Cfg>
 __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
   using P = Plan<Cfg>;
@@ -342,10 +348,14 @@ __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cf
         tc_fence_after_sync();
         const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
         const uint32_t sB = sA + P::A_BYTES;
+        // descriptors of the stage's first step; each further step only moves
+        // the start address (the low field, which no address here carries out of)
+        const uint64_t ad0 = operand_desc<Cfg::A_MN>(sA, 0);
+        const uint64_t bd0 = operand_desc<Cfg::B_MN>(sB, 0);
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          const uint64_t ad = operand_desc<Cfg::A_MN>(sA, kk);
-          const uint64_t bd = operand_desc<Cfg::B_MN>(sB, kk);
+          const uint64_t ad = ad0 + static_cast<uint64_t>(kk * operand_step<Cfg::A_MN>());
+          const uint64_t bd = bd0 + static_cast<uint64_t>(kk * operand_step<Cfg::B_MN>());
           const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
           if (P::PAIR)
             umma_bf16_f32_pair(d_tmem, ad, bd, idesc, acc);
