@@ -482,9 +482,17 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
         return fail_cuda(__LINE__);
     } else {
       CUtensorMap tm_dz, tm_w_mn;
+      const bool w_chunked = LLP_CHUNKED_MN && !LLP_HALF_TILE && (D % 64) == 0;  // half tiles load one chunk
       if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
-      if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
+      if (w_chunked) {
+        if (make_map_chunked(&tm_w_mn, weight, D, V, D * 2, llp::kTileK, llp::kBRows / 64, f16) != LLP_OK)
+          return fail_cuda(__LINE__);
+      } else if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) {
+        return fail_cuda(__LINE__);
+      }
       llp::GradGemmParams p;
+      p.a_chunked = 0;
+      p.b_chunked = w_chunked ? 1 : 0;
       p.rows = static_cast<int>(N);
       p.D = static_cast<int>(D);
       p.K = static_cast<int>(V);
@@ -498,6 +506,9 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       p.f32_out = f32_out ? 1 : 0;
       p.f16 = f16 ? 1 : 0;
       p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 0 : nullptr;
+      p.progress = (LLP_LOCKSTEP > 0 && (LLP_LOCKSTEP_MASK & 1) && p.sched != nullptr)
+                       ? reinterpret_cast<unsigned int*>(sched + 2)
+                       : nullptr;
       const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
       CUtensorMap tm_out;
       if (make_map_grad_out(&tm_out, p) != LLP_OK) return fail_cuda(__LINE__);
@@ -519,9 +530,24 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   // B3: grad_weight = dz^T . h over fixed token segments
   if (grad_weight != nullptr) {
     CUtensorMap tm_dz_mn, tm_h_mn;
-    if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
-    if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) return fail_cuda(__LINE__);
+    // dz rows are V_pad long with zero padding columns: whole 64-column chunks
+    const bool dz_chunked = LLP_CHUNKED_MN != 0;
+    const bool h_chunked = LLP_CHUNKED_MN && !LLP_HALF_TILE && (D % 64) == 0;
+    if (dz_chunked) {
+      if (make_map_chunked(&tm_dz_mn, dz, V_pad, N, V_pad * 2, llp::kTileK, llp::kTileM / 64, f16) != LLP_OK)
+        return fail_cuda(__LINE__);
+    } else if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) {
+      return fail_cuda(__LINE__);
+    }
+    if (h_chunked) {
+      if (make_map_chunked(&tm_h_mn, hidden, D, N, D * 2, llp::kTileK, llp::kBRows / 64, f16) != LLP_OK)
+        return fail_cuda(__LINE__);
+    } else if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) {
+      return fail_cuda(__LINE__);
+    }
     llp::GradGemmParams p;
+    p.a_chunked = dz_chunked ? 1 : 0;
+    p.b_chunked = h_chunked ? 1 : 0;
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
     p.K = static_cast<int>(N);
@@ -535,6 +561,9 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.f16 = f16 ? 1 : 0;
     p.err = dev->status_ptr;
     p.sched = !force_static_schedule() && max_unit_kblocks(p) >= llp::kDynMinKBlocks ? sched + 1 : nullptr;
+    p.progress = (LLP_LOCKSTEP > 0 && (LLP_LOCKSTEP_MASK & 2) && p.sched != nullptr)
+                     ? reinterpret_cast<unsigned int*>(sched + 3)
+                     : nullptr;
     const int64_t units = static_cast<int64_t>(p.nseg) * p.num_m * p.num_d;
     CUtensorMap tm_out;
     if (make_map_grad_out(&tm_out, p) != LLP_OK) return fail_cuda(__LINE__);

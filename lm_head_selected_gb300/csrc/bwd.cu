@@ -89,6 +89,9 @@ struct DzCfg {
   static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
   static constexpr bool DYNAMIC = false;
   static __device__ __forceinline__ int* sched_counter(const Params&) { return nullptr; }
+  static __device__ __forceinline__ unsigned int* progress_counter(const Params&) { return nullptr; }
+  static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
+  static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
   // the gradient GEMMs that follow on the stream start from ticket 0
   static __device__ __forceinline__ void on_launch(const Params& p) {
     if (p.sched_reset != nullptr)
@@ -232,6 +235,9 @@ struct GradCfg {
   // that share A rows or a K window of B run together
   static constexpr bool DYNAMIC = (LLP_DYNAMIC_SCHED & (A_MN ? 2 : 1)) != 0;
   static __device__ __forceinline__ int* sched_counter(const Params& p) { return p.sched; }
+  static __device__ __forceinline__ unsigned int* progress_counter(const Params& p) { return p.progress; }
+  static __device__ __forceinline__ bool a_chunked(const Params& p) { return p.a_chunked != 0; }
+  static __device__ __forceinline__ bool b_chunked(const Params& p) { return p.b_chunked != 0; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.nseg * p.num_m * p.num_d; }

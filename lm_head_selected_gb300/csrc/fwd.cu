@@ -55,6 +55,9 @@ struct FwdCfg {
   static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
   static constexpr bool DYNAMIC = false;
   static __device__ __forceinline__ int* sched_counter(const Params&) { return nullptr; }
+  static __device__ __forceinline__ unsigned int* progress_counter(const Params&) { return nullptr; }
+  static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
+  static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.num_m * p.num_splits; }

@@ -41,7 +41,11 @@
 // Operand layouts (both 128-byte swizzled, as TMA writes them):
 //   K-major  : box {64 K, R rows}; row pitch 128 B; 8-row groups 1024 B apart.
 //   MN-major : R/64 boxes {64 MN, 64 K}, each 8 KB; 8-K-row groups 1024 B apart,
-//              64-element MN chunks 8 KB apart.
+//              64-element MN chunks 8 KB apart.  When the MN extent is a whole
+//              number of 64-element chunks the operand comes as one 3-D copy
+//              {64, 64 K, R/64 chunks} (the map's third dimension steps over
+//              the chunks of a row), which lands in exactly that layout: an SM
+//              issues only so many tensor copies per microsecond.
 #pragma once
 
 #include "llp_internal.h"
@@ -68,6 +72,8 @@ struct UnitInfo {
 };
 
 constexpr int kSchedDepth = 4;  // unit-id slots between the ticket drawer and the other roles
+constexpr int kLockChunk = 16;                     // k-blocks between progress reports (advisory lockstep)
+constexpr unsigned long long kLockMaxWaitNs = 20000;  // longest nap per report
 
 template <class Cfg>
 struct Plan {
@@ -239,6 +245,15 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
   const bool dyn = Cfg::DYNAMIC && Cfg::sched_counter(p) != nullptr;
   int ticket = 0;
   if (dyn && leader) ticket = atomicAdd(Cfg::sched_counter(p), 1);
+  // Advisory lockstep of in-order units: every kLockChunk k-blocks the pair adds
+  // them to a shared progress counter and, while it is more than the window
+  // ahead of the mean over all pairs, naps (at most kLockMaxWaitNs per check,
+  // then goes on regardless).  Units that share operands then stream the same
+  // K window at the same time and meet in L2.  Scheduling only: no wait here
+  // decides anything about the arithmetic.
+  unsigned int* const prog = dyn && leader ? Cfg::progress_counter(p) : nullptr;
+  const unsigned int npairs = gridDim.x / P::NCTA;
+  unsigned int mine = 0;
   for (int k = 0;; ++k) {
     int u;
     if (dyn)
@@ -258,6 +273,21 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
         // latency hides behind the loads still to issue
         if (dyn && leader && j == ui.ntiles - 1 && kb == (ui.nkb > 4 ? ui.nkb - 4 : 0))
           ticket = atomicAdd(Cfg::sched_counter(p), 1);
+        if (prog != nullptr && ((kb + 1) % kLockChunk) == 0) {
+          mine += kLockChunk;
+          unsigned int total = atomicAdd(prog, static_cast<unsigned int>(kLockChunk)) + kLockChunk;
+          // the last wave runs free: pairs without units stop reporting
+          if (u + static_cast<int>(npairs) < num_units) {
+            const unsigned long long t0 = global_timer_ns();
+            const unsigned int win = static_cast<unsigned int>(LLP_LOCKSTEP);
+            while (static_cast<unsigned long long>(mine) * npairs >
+                   static_cast<unsigned long long>(total) + static_cast<unsigned long long>(win) * npairs) {
+              if (global_timer_ns() - t0 > kLockMaxWaitNs) break;
+              __nanosleep(256);
+              total = *reinterpret_cast<volatile unsigned int*>(prog);
+            }
+          }
+        }
         if (!mbar_wait(&st.empty[stage], phase ^ 1u, st.abort, st.err, kDevTimeoutEmpty)) return;
         const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
         const uint32_t sB = sA + P::A_BYTES;
@@ -267,12 +297,16 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
           const uint32_t bar = map_to_cta(smem_u32(&st.full[stage]), 0);
           if (!Cfg::A_MN) {
             tma_load_2d_pair(sA, tmA, bar, kx, a_row, polA);
+          } else if (Cfg::a_chunked(p)) {
+            tma_load_3d_pair(sA, tmA, bar, 0, kx, a_row / 64, polA);
           } else {
 #pragma unroll
             for (int i = 0; i < BM / 64; ++i) tma_load_2d_pair(sA + i * 8192, tmA, bar, a_row + 64 * i, kx, polA);
           }
           if (!Cfg::B_MN) {
             tma_load_2d_pair(sB, tmB, bar, kx, b_row, polB);
+          } else if (Cfg::b_chunked(p)) {
+            tma_load_3d_pair(sB, tmB, bar, 0, kx, b_row / 64, polB);
           } else {
             for (int i = 0; i < b_rows / 64; ++i) tma_load_2d_pair(sB + i * 8192, tmB, bar, b_row + 64 * i, kx, polB);
           }
@@ -280,6 +314,8 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
           mbar_arrive_expect_tx(&st.full[stage], tx);
           if (!Cfg::A_MN) {
             tma_load_2d(sA, tmA, &st.full[stage], kx, a_row, polA);
+          } else if (Cfg::a_chunked(p)) {
+            tma_load_3d(sA, tmA, &st.full[stage], 0, kx, a_row / 64, polA);
           } else {
 #pragma unroll
             for (int i = 0; i < BM / 64; ++i)
@@ -287,6 +323,8 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
           }
           if (!Cfg::B_MN) {
             tma_load_2d(sB, tmB, &st.full[stage], kx, b_row, polB);
+          } else if (Cfg::b_chunked(p)) {
+            tma_load_3d(sB, tmB, &st.full[stage], 0, kx, b_row / 64, polB);
           } else {
             for (int i = 0; i < b_rows / 64; ++i)
               tma_load_2d(sB + i * 8192, tmB, &st.full[stage], b_row + 64 * i, kx, polB);

@@ -43,6 +43,15 @@ constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 #ifndef LLP_EPI_FASTEXP
 #define LLP_EPI_FASTEXP 1    // GEMM epilogues: the ex2.approx.ftz instruction instead of exp2f
 #endif
+#ifndef LLP_LOCKSTEP
+#define LLP_LOCKSTEP 0       // gradient GEMMs: pairs report progress and wait when too far ahead (k-block window, 0 = off)
+#endif
+#ifndef LLP_LOCKSTEP_MASK
+#define LLP_LOCKSTEP_MASK 3  // bit 0: grad_hidden, bit 1: grad_weight take part in the lockstep
+#endif
+#ifndef LLP_CHUNKED_MN
+#define LLP_CHUNKED_MN 1     // MN-major GEMM operands as one 3-D copy per stage (when MN % 64 == 0)
+#endif
 #ifndef LLP_HALF_TILE
 #define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
 #endif
@@ -126,9 +135,9 @@ struct DzParams {
 };
 
 // Ticket counters of the in-order scheduled gradient GEMMs (one per GEMM of a
-// backward), held in the backward workspace and zeroed by the dlogits kernel
-// that precedes them on the stream.
-constexpr int kNumSchedCounters = 2;
+// backward) and their progress counters, held in the backward workspace and
+// zeroed by the dlogits kernel that precedes them on the stream.
+constexpr int kNumSchedCounters = 4;
 
 struct GradGemmParams {
   int rows;          // M extent: N for grad_hidden, V for grad_weight
@@ -140,6 +149,8 @@ struct GradGemmParams {
   unsigned int* err;
   int f32_out;         // 1: always write fp32 partials (a vocab shard's grad_hidden contribution)
   int* sched;          // ticket counter, 0 at launch; nullptr: round-robin units
+  unsigned int* progress;  // k-blocks issued by all pairs, 0 at launch (advisory lockstep); nullptr: off
+  int a_chunked, b_chunked;  // the MN-major operand's map is 3-D {64, K, MN/64}: one copy per stage
   int f16;             // operands and the 16-bit output are IEEE fp16 (else bf16)
 };
 
