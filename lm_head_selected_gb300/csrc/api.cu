@@ -321,6 +321,26 @@ RowTiling row_tiling(int64_t N) {
   return {single, single ? llp::kTileM : llp::kUnitM, single ? llp::kTileN : llp::kBRows};
 }
 
+// K-blocks per pipeline stage of the forward / dlogits GEMMs: two (one 3-D copy
+// per operand per stage) on CTA pairs when the hidden size is whole 64-column
+// chunks.  The single-CTA tiling of small batches streams the weight from HBM
+// and keeps its four one-k-block stages: two double-size stages leave only one
+// in flight while the MMAs read the other.
+int k_blocks_per_stage(int64_t D, bool single) { return ((LLP_KPS2 & 1) && !single && (D % 64) == 0) ? 2 : 1; }
+
+// Tensor maps of the two K-major operands of the forward / dlogits GEMMs, the
+// hidden states (box rows kTileM) and the weight (box rows w_box_rows): 2-D with
+// a 64-wide K box, or, with kps == 2, 3-D over 64-column K chunks, two chunks per box.
+int make_kmajor_maps(CUtensorMap* tm_h, CUtensorMap* tm_w, const void* hidden, const void* weight, int64_t N,
+                     int64_t D, int64_t V, int w_box_rows, int kps, bool f16) {
+  if (kps == 2) {
+    if (make_map_chunked(tm_h, hidden, D, N, D * 2, llp::kTileM, 2, f16) != LLP_OK) return LLP_ERR_CUDA;
+    return make_map_chunked(tm_w, weight, D, V, D * 2, w_box_rows, 2, f16);
+  }
+  if (make_map(tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
+  return make_map(tm_w, weight, D, V, D * 2, llp::kTileK, w_box_rows, f16);
+}
+
 // Forward launch sequence on validated arguments (N > 0, workspace sized by fwd_layout).
 // With sh_max set, `weight` is a vocab shard whose row 0 is global id vocab_start,
 // and the shard's (max, sum, target logit) triple is written instead of logp / lse.
@@ -331,8 +351,9 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   const FwdLayout L = fwd_layout(N, V);
   const RowTiling T = row_tiling(N);
   CUtensorMap tm_h, tm_w;
-  if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
-  if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, T.w_box_rows, f16) != LLP_OK) return fail_cuda(__LINE__);
+  const int kps = k_blocks_per_stage(D, T.single);
+  if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16) != LLP_OK)
+    return fail_cuda(__LINE__);
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
@@ -352,6 +373,7 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.vocab_start = vocab_start;
   p.global_V = V;
   p.f16 = f16 ? 1 : 0;
+  p.kps = kps;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
   rec_mark(s, -1);
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s, T.single) != cudaSuccess) return fail_cuda(__LINE__);
@@ -415,8 +437,9 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
   const RowTiling T = row_tiling(N);
   {
     CUtensorMap tm_h, tm_w;
-    if (make_map(&tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
-    if (make_map(&tm_w, weight, D, V, D * 2, llp::kTileK, T.w_box_rows, f16) != LLP_OK) return fail_cuda(__LINE__);
+    const int kps = k_blocks_per_stage(D, T.single);
+    if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16) != LLP_OK)
+      return fail_cuda(__LINE__);
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -438,6 +461,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.global_V = global_V;
     p.sched_reset = sched;
     p.f16 = f16 ? 1 : 0;
+    p.kps = kps;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
     rec_mark(s, -1);
     // dz [N][V_pad], written in 64 x 32 slabs; the columns [V, V_pad) of the last
@@ -483,9 +507,16 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     } else {
       CUtensorMap tm_dz, tm_w_mn;
       const bool w_chunked = LLP_CHUNKED_MN && !LLP_HALF_TILE && (D % 64) == 0;  // half tiles load one chunk
-      if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return fail_cuda(__LINE__);
+      // dz rows are V_pad long with zero padding columns: whole 64-column K chunks
+      const int kps = ((LLP_KPS2 & 2) && w_chunked) ? 2 : 1;
+      if (kps == 2) {
+        if (make_map_chunked(&tm_dz, dz, V_pad, N, V_pad * 2, llp::kTileM, 2, f16) != LLP_OK)
+          return fail_cuda(__LINE__);
+      } else if (make_map(&tm_dz, dz, V, N, V_pad * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) {
+        return fail_cuda(__LINE__);
+      }
       if (w_chunked) {
-        if (make_map_chunked(&tm_w_mn, weight, D, V, D * 2, llp::kTileK, llp::kBRows / 64, f16) != LLP_OK)
+        if (make_map_chunked(&tm_w_mn, weight, D, V, D * 2, llp::kTileK * kps, llp::kBRows / 64, f16) != LLP_OK)
           return fail_cuda(__LINE__);
       } else if (make_map(&tm_w_mn, weight, D, V, D * 2, 64, llp::kTileK, f16) != LLP_OK) {
         return fail_cuda(__LINE__);
@@ -493,6 +524,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       llp::GradGemmParams p;
       p.a_chunked = 0;
       p.b_chunked = w_chunked ? 1 : 0;
+      p.kps = kps;
       p.rows = static_cast<int>(N);
       p.D = static_cast<int>(D);
       p.K = static_cast<int>(V);
@@ -533,14 +565,17 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     // dz rows are V_pad long with zero padding columns: whole 64-column chunks
     const bool dz_chunked = LLP_CHUNKED_MN != 0;
     const bool h_chunked = LLP_CHUNKED_MN && !LLP_HALF_TILE && (D % 64) == 0;
+    // a unit's K is at most one token segment: with few tokens the second
+    // k-block of a stage would mostly be padding
+    const int kps = ((LLP_KPS2 & 4) && dz_chunked && h_chunked && N >= 1024) ? 2 : 1;
     if (dz_chunked) {
-      if (make_map_chunked(&tm_dz_mn, dz, V_pad, N, V_pad * 2, llp::kTileK, llp::kTileM / 64, f16) != LLP_OK)
+      if (make_map_chunked(&tm_dz_mn, dz, V_pad, N, V_pad * 2, llp::kTileK * kps, llp::kTileM / 64, f16) != LLP_OK)
         return fail_cuda(__LINE__);
     } else if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) {
       return fail_cuda(__LINE__);
     }
     if (h_chunked) {
-      if (make_map_chunked(&tm_h_mn, hidden, D, N, D * 2, llp::kTileK, llp::kBRows / 64, f16) != LLP_OK)
+      if (make_map_chunked(&tm_h_mn, hidden, D, N, D * 2, llp::kTileK * kps, llp::kBRows / 64, f16) != LLP_OK)
         return fail_cuda(__LINE__);
     } else if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) {
       return fail_cuda(__LINE__);
@@ -548,6 +583,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     llp::GradGemmParams p;
     p.a_chunked = dz_chunked ? 1 : 0;
     p.b_chunked = h_chunked ? 1 : 0;
+    p.kps = kps;
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
     p.K = static_cast<int>(N);

@@ -92,6 +92,7 @@ struct DzCfg {
   static __device__ __forceinline__ unsigned int* progress_counter(const Params&) { return nullptr; }
   static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
   static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
+  static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
   // the gradient GEMMs that follow on the stream start from ticket 0
   static __device__ __forceinline__ void on_launch(const Params& p) {
     if (p.sched_reset != nullptr)
@@ -238,6 +239,7 @@ struct GradCfg {
   static __device__ __forceinline__ unsigned int* progress_counter(const Params& p) { return p.progress; }
   static __device__ __forceinline__ bool a_chunked(const Params& p) { return p.a_chunked != 0; }
   static __device__ __forceinline__ bool b_chunked(const Params& p) { return p.b_chunked != 0; }
+  static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.nseg * p.num_m * p.num_d; }

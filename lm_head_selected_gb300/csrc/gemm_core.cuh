@@ -232,13 +232,18 @@ __device__ __forceinline__ int static_unit(const SharedState& st, const typename
 // ----------------------------------------------------------------------------
 // Producer: one lane of warp 0 in every CTA.
 // ----------------------------------------------------------------------------
-template <class Cfg>
-__device__ __forceinline__ void run_producer(const SharedState& st, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                             const typename Cfg::Params& p) {
+// kps: k-blocks per stage, 1, or 2 when both operands come as 3-D copies of two
+// k-blocks each (one copy per operand per stage; same bytes in flight).  A
+// template parameter, so that each form compiles to straight-line code.
+template <class Cfg, int kps>
+__device__ __forceinline__ void run_producer_k(const SharedState& st, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                               const typename Cfg::Params& p) {
   using P = Plan<Cfg>;
   const uint64_t polA = Cfg::policy_a();
   const uint64_t polB = Cfg::policy_b();
   const bool leader = st.rank == 0;
+  constexpr int nstages = Cfg::STAGES / kps;
+  constexpr int stage_bytes = P::STAGE_BYTES * kps;
   int stage = 0;
   uint32_t phase = 0;
   const int num_units = Cfg::num_units(p);
@@ -265,15 +270,16 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
     const int a_row = ui.m0 + static_cast<int>(st.rank) * BM;
     // B rows this CTA loads per k-block: half of the unit's N in pair mode
     const int b_rows = P::PAIR ? ui.bn / 2 : ui.bn;
-    const uint32_t tx = static_cast<uint32_t>(P::NCTA * (P::A_BYTES + b_rows * BK * 2));
+    const uint32_t tx = static_cast<uint32_t>(P::NCTA * (P::A_BYTES + b_rows * BK * 2) * kps);
+    // draw the next ticket a few k-blocks before the unit ends, so its latency
+    // hides behind the loads still to issue
+    const int draw_at = ui.nkb > 4 ? ui.nkb - 4 : 0;
     for (int j = 0; j < ui.ntiles; ++j) {
       const int b_row = ui.n0 + j * Cfg::BN + static_cast<int>(st.rank) * b_rows;
-      for (int kb = 0; kb < ui.nkb; ++kb) {
-        // draw the next ticket a few k-blocks before the unit ends, so its
-        // latency hides behind the loads still to issue
-        if (dyn && leader && j == ui.ntiles - 1 && kb == (ui.nkb > 4 ? ui.nkb - 4 : 0))
+      for (int kb = 0; kb < ui.nkb; kb += kps) {
+        if (dyn && leader && j == ui.ntiles - 1 && kb <= draw_at && draw_at < kb + kps)
           ticket = atomicAdd(Cfg::sched_counter(p), 1);
-        if (prog != nullptr && ((kb + 1) % kLockChunk) == 0) {
+        if (prog != nullptr && ((kb + kps) % kLockChunk) == 0) {
           mine += kLockChunk;
           unsigned int total = atomicAdd(prog, static_cast<unsigned int>(kLockChunk)) + kLockChunk;
           // the last wave runs free: pairs without units stop reporting
@@ -289,14 +295,19 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
           }
         }
         if (!mbar_wait(&st.empty[stage], phase ^ 1u, st.abort, st.err, kDevTimeoutEmpty)) return;
-        const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
-        const uint32_t sB = sA + P::A_BYTES;
+        const uint32_t sA = smem_u32(st.tiles + stage * stage_bytes);
+        const uint32_t sB = sA + P::A_BYTES * kps;
         const int kx = (ui.kb0 + kb) * BK;
+        // K-major with kps == 2: the 3-D map's third dimension steps over 64-wide
+        // K chunks; MN-major chunked: over 64-wide MN chunks, K rows in the box
         if (P::PAIR) {
           if (leader) mbar_arrive_expect_tx(&st.full[stage], tx);
           const uint32_t bar = map_to_cta(smem_u32(&st.full[stage]), 0);
           if (!Cfg::A_MN) {
-            tma_load_2d_pair(sA, tmA, bar, kx, a_row, polA);
+            if (kps == 2)
+              tma_load_3d_pair(sA, tmA, bar, 0, a_row, kx / 64, polA);
+            else
+              tma_load_2d_pair(sA, tmA, bar, kx, a_row, polA);
           } else if (Cfg::a_chunked(p)) {
             tma_load_3d_pair(sA, tmA, bar, 0, kx, a_row / 64, polA);
           } else {
@@ -304,7 +315,10 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
             for (int i = 0; i < BM / 64; ++i) tma_load_2d_pair(sA + i * 8192, tmA, bar, a_row + 64 * i, kx, polA);
           }
           if (!Cfg::B_MN) {
-            tma_load_2d_pair(sB, tmB, bar, kx, b_row, polB);
+            if (kps == 2)
+              tma_load_3d_pair(sB, tmB, bar, 0, b_row, kx / 64, polB);
+            else
+              tma_load_2d_pair(sB, tmB, bar, kx, b_row, polB);
           } else if (Cfg::b_chunked(p)) {
             tma_load_3d_pair(sB, tmB, bar, 0, kx, b_row / 64, polB);
           } else {
@@ -313,7 +327,10 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
         } else {
           mbar_arrive_expect_tx(&st.full[stage], tx);
           if (!Cfg::A_MN) {
-            tma_load_2d(sA, tmA, &st.full[stage], kx, a_row, polA);
+            if (kps == 2)
+              tma_load_3d(sA, tmA, &st.full[stage], 0, a_row, kx / 64, polA);
+            else
+              tma_load_2d(sA, tmA, &st.full[stage], kx, a_row, polA);
           } else if (Cfg::a_chunked(p)) {
             tma_load_3d(sA, tmA, &st.full[stage], 0, kx, a_row / 64, polA);
           } else {
@@ -322,7 +339,10 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
               tma_load_2d(sA + i * 8192, tmA, &st.full[stage], a_row + 64 * i, kx, polA);
           }
           if (!Cfg::B_MN) {
-            tma_load_2d(sB, tmB, &st.full[stage], kx, b_row, polB);
+            if (kps == 2)
+              tma_load_3d(sB, tmB, &st.full[stage], 0, b_row, kx / 64, polB);
+            else
+              tma_load_2d(sB, tmB, &st.full[stage], kx, b_row, polB);
           } else if (Cfg::b_chunked(p)) {
             tma_load_3d(sB, tmB, &st.full[stage], 0, kx, b_row / 64, polB);
           } else {
@@ -330,7 +350,7 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
               tma_load_2d(sB + i * 8192, tmB, &st.full[stage], b_row + 64 * i, kx, polB);
           }
         }
-        if (++stage == Cfg::STAGES) {
+        if (++stage == nstages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -339,29 +359,45 @@ __device__ __forceinline__ void run_producer(const SharedState& st, const CUtens
   }
 }
 
+template <class Cfg>
+__device__ __forceinline__ void run_producer(const SharedState& st, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                             const typename Cfg::Params& p) {
+  if (Cfg::kps(p) == 2 && Cfg::STAGES % 2 == 0)
+    run_producer_k<Cfg, 2>(st, tmA, tmB, p);
+  else
+    run_producer_k<Cfg, 1>(st, tmA, tmB, p);
+}
+
 // ----------------------------------------------------------------------------
 // MMA issuer: one lane of warp 1 (of the even CTA in pair mode).
 // ----------------------------------------------------------------------------
+// Descriptor of a stage's operand at its first 16-deep step.  K-major: rows of
+// 128 bytes, 8-row groups 1024 B apart.  MN-major: 8-K-row groups 1024 B apart,
+// 64-element MN chunks (64 * kps K rows of 128 B each) further on.
 template <bool MN>
-__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
-  // K-major: advancing K by 16 bf16 = 32 bytes inside the 128-byte swizzle row.
-  // MN-major: advancing K by 16 rows = 16 * 128 bytes; MN chunks 8 KB apart.
-  return MN ? make_smem_desc_sw128(base + kk * (UMMA_K * 128), 8192, 1024)
-            : make_smem_desc_sw128(base + kk * (UMMA_K * 2), 16, 1024);
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kps) {
+  return MN ? make_smem_desc_sw128(base, 8192u * static_cast<uint32_t>(kps), 1024)
+            : make_smem_desc_sw128(base, 16, 1024);
 }
 
-// How far operand_desc's start-address field moves per 16-deep step (16-byte units).
+// How far the start-address field (16-byte units) moves for step kk (0..3) of
+// the stage's k-block c: K-major, 32 bytes per step inside the swizzle row and
+// a whole k-block tile (rows x 128 B) per k-block; MN-major, 16 K rows of 128 B
+// per step.
 template <bool MN>
-__device__ __forceinline__ constexpr int operand_step() {
-  return MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
+__device__ __forceinline__ uint32_t operand_offset(int c, int kk, int rows) {
+  return MN ? static_cast<uint32_t>(((c * 4 + kk) * UMMA_K * 128) >> 4)
+            : static_cast<uint32_t>((c * rows * 128 + kk * UMMA_K * 2) >> 4);
 }
 
-template <class Cfg>
-__device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
+template <class Cfg, int kps>
+__device__ __forceinline__ void run_mma_k(const SharedState& st, const typename Cfg::Params& p) {
   using P = Plan<Cfg>;
   // both operands have the same 16-bit type (the params' f16 flag)
   const uint32_t idesc_full = make_idesc_16_f32(P::UM, Cfg::BN, Cfg::A_MN, Cfg::B_MN, p.f16 != 0);
   const uint32_t idesc_half = make_idesc_16_f32(P::UM, Cfg::BN / 2, Cfg::A_MN, Cfg::B_MN, p.f16 != 0);
+  constexpr int nstages = Cfg::STAGES / kps;
+  constexpr int stage_bytes = P::STAGE_BYTES * kps;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t acc_i = 0;
@@ -381,31 +417,34 @@ __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cf
       if (!mbar_wait(&st.tmem_empty[buf], acc_phase ^ 1u, st.abort, st.err, kDevTimeoutTmemEmpty)) return;
       tc_fence_after_sync();
       const uint32_t d_tmem = st.tmem_base + buf * Cfg::BN;
-      for (int kb = 0; kb < ui.nkb; ++kb) {
+      for (int kb = 0; kb < ui.nkb; kb += kps) {
         if (!mbar_wait(&st.full[stage], phase, st.abort, st.err, kDevTimeoutFull)) return;
         tc_fence_after_sync();
-        const uint32_t sA = smem_u32(st.tiles + stage * P::STAGE_BYTES);
-        const uint32_t sB = sA + P::A_BYTES;
+        const uint32_t sA = smem_u32(st.tiles + stage * stage_bytes);
+        const uint32_t sB = sA + P::A_BYTES * kps;
         // descriptors of the stage's first step; each further step only moves
         // the start address (the low field, which no address here carries out of)
-        const uint64_t ad0 = operand_desc<Cfg::A_MN>(sA, 0);
-        const uint64_t bd0 = operand_desc<Cfg::B_MN>(sB, 0);
+        const uint64_t ad0 = operand_desc<Cfg::A_MN>(sA, kps);
+        const uint64_t bd0 = operand_desc<Cfg::B_MN>(sB, kps);
 #pragma unroll
-        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          const uint64_t ad = ad0 + static_cast<uint64_t>(kk * operand_step<Cfg::A_MN>());
-          const uint64_t bd = bd0 + static_cast<uint64_t>(kk * operand_step<Cfg::B_MN>());
-          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          if (P::PAIR)
-            umma_bf16_f32_pair(d_tmem, ad, bd, idesc, acc);
-          else
-            umma_bf16_f32(d_tmem, ad, bd, idesc, acc);
+        for (int c = 0; c < kps; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t ad = ad0 + operand_offset<Cfg::A_MN>(c, kk, BM);
+            const uint64_t bd = bd0 + operand_offset<Cfg::B_MN>(c, kk, P::B_ROWS);
+            const uint32_t acc = (kb > 0 || c > 0 || kk > 0) ? 1u : 0u;
+            if (P::PAIR)
+              umma_bf16_f32_pair(d_tmem, ad, bd, idesc, acc);
+            else
+              umma_bf16_f32(d_tmem, ad, bd, idesc, acc);
+          }
         }
         // frees the stage (in both CTAs) once these MMAs have read it
         if (P::PAIR)
           umma_commit_pair_multicast(&st.empty[stage], 0x3);
         else
           umma_commit(&st.empty[stage]);
-        if (++stage == Cfg::STAGES) {
+        if (++stage == nstages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -417,6 +456,14 @@ __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cf
         umma_commit(&st.tmem_full[buf]);
     }
   }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
+  if (Cfg::kps(p) == 2 && Cfg::STAGES % 2 == 0)
+    run_mma_k<Cfg, 2>(st, p);
+  else
+    run_mma_k<Cfg, 1>(st, p);
 }
 
 // ----------------------------------------------------------------------------

@@ -52,6 +52,10 @@ constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 #ifndef LLP_CHUNKED_MN
 #define LLP_CHUNKED_MN 1     // MN-major GEMM operands as one 3-D copy per stage (when MN % 64 == 0)
 #endif
+#ifndef LLP_KPS2
+#define LLP_KPS2 5           // two k-blocks per pipeline stage (one 3-D copy per operand) where the maps allow,
+                             // bit 0: forward / dlogits on CTA pairs, 1: grad_hidden, 2: grad_weight (>= 1024 tokens)
+#endif
 #ifndef LLP_HALF_TILE
 #define LLP_HALF_TILE 0      // half-width MMA for a last column tile with <= 128 columns
 #endif
@@ -114,6 +118,7 @@ struct FwdParams {
   long long vocab_start;  // global id of local vocab row 0 (vocab-parallel shards; 0 otherwise)
   long long global_V;     // global vocab size (== V unless sharded)
   int f16;                // hidden / weight are IEEE fp16 (else bf16)
+  int kps;                // k-blocks per pipeline stage: 2 with 3-D chunked maps (D % 64 == 0), else 1
 };
 
 struct DzParams {
@@ -132,6 +137,7 @@ struct DzParams {
   long long global_V;     // global vocab size: decides which targets are valid
   int* sched_reset;       // [kNumSchedCounters] ticket counters of the gradient GEMMs, zeroed at launch
   int f16;                // hidden / weight / dz are IEEE fp16 (else bf16)
+  int kps;                // k-blocks per pipeline stage: 2 with 3-D chunked maps (D % 64 == 0), else 1
 };
 
 // Ticket counters of the in-order scheduled gradient GEMMs (one per GEMM of a
@@ -151,6 +157,7 @@ struct GradGemmParams {
   int* sched;          // ticket counter, 0 at launch; nullptr: round-robin units
   unsigned int* progress;  // k-blocks issued by all pairs, 0 at launch (advisory lockstep); nullptr: off
   int a_chunked, b_chunked;  // the MN-major operand's map is 3-D {64, K, MN/64}: one copy per stage
+  int kps;             // k-blocks per pipeline stage: 2 when every operand map is 3-D, else 1
   int f16;             // operands and the 16-bit output are IEEE fp16 (else bf16)
 };
 
