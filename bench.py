@@ -72,10 +72,11 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by sources_sha).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "3899ed93af41766f",
-    "how": "dram__bytes_read.sum + dram__bytes_write.sum of one launch per kernel, full-size workload, one box",
-    "bytes_per_launch": {"fwd_partials": 2169387264 + 37225728, "dlogits": 6398021376 + 4268878336,
-                         "grad_hidden": 24050236672 + 694915840, "grad_weight": 16667673088 + 701035264},
+    "sources_sha": "cffffbed9acc246e",
+    "how": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch per kernel (ncu -k one kernel, -c 1, "
+            "1 pass), full-size workload, one box; box-to-box spread for the same build is large"),
+    "bytes_per_launch": {"fwd_partials": 3386685440 + 36863232, "dlogits": 5744539136 + 4283281152,
+                         "grad_hidden": 28047893504 + 702404608, "grad_weight": 11465787392 + 702200320},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
