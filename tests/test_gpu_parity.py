@@ -51,6 +51,10 @@ SHAPES = [
     (257, 512, 2048, False, True, 0, 0),  # three M tiles, the last with one row
     (33, 64, 131073, False, True, 1, 0),  # 257 vocab splits: the split merge takes a second round of one split
     (40, 64, 200000, True, False, 2, 1),  # 391 vocab splits, ragged last split
+    # >= 1024 tokens: grad_weight takes two k-blocks per stage; D = 3 x 64 is an odd number of 64-column
+    # chunks, so a copy's second chunk of hidden runs past D (read as zeros)
+    (1100, 192, 3000, True, True, 3, 1),
+    (1030, 200, 2500, False, True, 2, 0),  # D not a multiple of 64: every GEMM on one k-block per stage, 2-D maps
 ]
 
 
