@@ -362,7 +362,7 @@ __device__ __forceinline__ void run_producer_k(const SharedState& st, const CUte
 template <class Cfg>
 __device__ __forceinline__ void run_producer(const SharedState& st, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                              const typename Cfg::Params& p) {
-  if (Cfg::kps(p) == 2 && Cfg::STAGES % 2 == 0)
+  if (Cfg::kps(p) == 2)  // STAGES / 2 double stages (an odd last buffer goes unused)
     run_producer_k<Cfg, 2>(st, tmA, tmB, p);
   else
     run_producer_k<Cfg, 1>(st, tmA, tmB, p);
@@ -460,7 +460,7 @@ __device__ __forceinline__ void run_mma_k(const SharedState& st, const typename 
 
 template <class Cfg>
 __device__ __forceinline__ void run_mma(const SharedState& st, const typename Cfg::Params& p) {
-  if (Cfg::kps(p) == 2 && Cfg::STAGES % 2 == 0)
+  if (Cfg::kps(p) == 2)
     run_mma_k<Cfg, 2>(st, p);
   else
     run_mma_k<Cfg, 1>(st, p);
