@@ -72,11 +72,11 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by sources_sha).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "cffffbed9acc246e",
+    "sources_sha": "e06004c466bb7265",
     "how": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch per kernel (ncu -k one kernel, -c 1, "
             "1 pass), full-size workload, one box; box-to-box spread for the same build is large"),
-    "bytes_per_launch": {"fwd_partials": 3386685440 + 36863232, "dlogits": 5744539136 + 4283281152,
-                         "grad_hidden": 28047893504 + 702404608, "grad_weight": 11465787392 + 702200320},
+    "bytes_per_launch": {"fwd_partials": 2952650240 + 36931072, "dlogits": 5211738368 + 4280860416,
+                         "grad_hidden": 23447700992 + 697505792, "grad_weight": 11419964160 + 700668160},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
