@@ -77,7 +77,15 @@ enum {
  * round-robin otherwise.  Which SM computes a unit never changes the
  * arithmetic, so results are bitwise the same either way; setting the
  * environment variable LINEAR_LOGP_SCHEDULE=static before the library's first
- * call forces round-robin everywhere (a diagnostic, read once per process). */
+ * call forces round-robin everywhere (a diagnostic, read once per process).
+ *
+ * Kernel-choice note: the backward of a batch of at most 128 rows computes
+ * grad_hidden with the hidden dimension on the tensor-core MMA's M side and the
+ * tokens on its N side (no padding rows are multiplied); larger batches use the
+ * two-CTA GEMM with the tokens on M.  Both accumulate every element over the
+ * same 16-wide vocab slices in the same order, so the results are bitwise the
+ * same; LINEAR_LOGP_SMALL_GRAD_HIDDEN=0 before the first call sends small
+ * batches through the two-CTA GEMM too (a diagnostic, read once per process). */
 
 /* Bytes of workspace linear_logp_fwd needs for an N x D x V problem
  * (0 when N == 0).  The workspace holds the per-vocab-split (max, sum) pairs

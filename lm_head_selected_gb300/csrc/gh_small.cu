@@ -49,8 +49,8 @@ constexpr int kSmThreads = 224;
 constexpr int kSmTmemCols = 256;  // two accumulators of up to 128 token columns
 constexpr int kSmBarBytes = 512;  // 4 rings of up to kSmallGhMaxStages barriers, 5 more, 2 words
 
-// Per stage the weight ring holds R vocab rows x 128 hidden columns (two
-// 64-column chunks of R x 128 bytes); a dz slot holds b_span stages' worth of
+// Per stage the weight ring holds kSmallGhRows vocab rows x 128 hidden columns
+// (two 64-column chunks of kSmallGhRows x 128 bytes); a dz slot holds b_span stages' worth of
 // vocab rows for all BN tokens.
 __host__ __device__ inline int sm_a_box(const GhSmallParams&) { return kSmallGhRows * 128; }
 __host__ __device__ inline int sm_a_stage(const GhSmallParams&) { return 2 * kSmallGhRows * 128; }
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
           }
           tc_fence_after_sync();
           // A (weight, MN-major): 16 vocab rows = 2 KB further per step; the
-          // second 64-column chunk is R x 128 bytes on.  B (dz, K-major):
+          // second 64-column chunk is kSmallGhRows x 128 bytes on.  B (dz, K-major):
           // 64-row vocab chunks of BN token rows, 32 bytes per 16-wide step
           // inside a chunk.
           const uint64_t ad0 =
