@@ -79,7 +79,7 @@ enum {
  * environment variable LINEAR_LOGP_SCHEDULE=static before the library's first
  * call forces round-robin everywhere (a diagnostic, read once per process).
  *
- * Kernel-choice note: the backward of a batch of at most 128 rows computes
+ * Kernel-choice note: the backward of a batch of at most 96 rows computes
  * grad_hidden with the hidden dimension on the tensor-core MMA's M side and the
  * tokens on its N side (no padding rows are multiplied); larger batches use the
  * two-CTA GEMM with the tokens on M.  Both accumulate every element over the

@@ -1,4 +1,4 @@
-// grad_hidden for small batches (at most kSmallGhMaxN token rows), with the
+// grad_hidden for small batches (at most kSmallGhMaxN = 96 token rows), with the
 // operands of the contraction swapped:
 //
 //     grad_hidden^T [D, N] = W^T [D, V] . dz^T [V, N]

@@ -66,7 +66,10 @@ constexpr int kDynMinKBlocks = LLP_DYN_MIN_KB;
 
 // grad_hidden of small batches with the hidden dimension on the MMA's M side
 // and the tokens on its N side (gh_small.cu).
-constexpr int kSmallGhMaxN = 128;        // largest batch it takes (tokens padded to a multiple of 16)
+// Largest batch it takes (tokens padded to a multiple of 16).  Above 96 tokens
+// a dz slot (256 vocab rows x tokens) is so large that only one fits beside two
+// weight stages, and the two-CTA GEMM is faster (N=112: 220 vs 160 us).
+constexpr int kSmallGhMaxN = 96;
 constexpr int kSmallGhRows = 256;        // vocab rows per weight stage (height of the weight boxes)
 constexpr int kSmallGhMaxStages = 8;     // deepest ring of either operand
 constexpr int kSmallGhSmemLimit = 232448;  // dynamic shared memory the kernel may use

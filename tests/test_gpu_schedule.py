@@ -60,7 +60,7 @@ def test_in_order_and_round_robin_schedules_agree_bitwise(tmp_path):
     assert torch.equal(gb.cpu(), ref["gb"])
 
 
-# grad_hidden of batches of at most 128 rows runs on the swapped-operand kernel
+# grad_hidden of batches of at most 96 rows runs on the swapped-operand kernel
 # (hidden on the MMA's M side, tokens on N); LINEAR_LOGP_SMALL_GRAD_HIDDEN=0 (read
 # once per process) sends them through the CTA-pair GEMM.  Both accumulate every
 # element over the same 16-wide vocab slices in the same order.
@@ -68,7 +68,8 @@ SMALL_CASES = [
     # (N, D, V, bias, temperature, fp16)
     (32, 2688, 131072, False, True, False),   # the Nemotron head at batch 2 x seq 16
     (17, 264, 50257, True, True, False),      # D not a multiple of 128, V not a multiple of 64
-    (128, 512, 33000, False, False, False),   # the largest batch the kernel takes (one dz slot)
+    (96, 512, 33000, False, False, False),    # the largest batch the kernel takes (two dz slots, two weight stages)
+    (128, 512, 33000, False, False, False),   # above it: both processes run the CTA-pair GEMM
     (100, 256, 40000, True, False, True),     # fp16 inputs
     (1, 128, 70000, False, False, False),     # a single token, three vocab segments
 ]
