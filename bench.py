@@ -50,6 +50,10 @@ WORKLOADS = {
     "nemotron_n32": (32, 2688, 131072,
                      "Nemotron-3-Nano LM head, N=32 (2x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
                      "uniform targets, grad_logp=1"),
+    # batch 1 x seq 16 on the same head: the GEMMs read per-CTA copies of the hidden states
+    "nemotron_n16": (16, 2688, 131072,
+                     "Nemotron-3-Nano LM head, N=16 (1x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
+                     "uniform targets, grad_logp=1"),
     # the tiny correctness configuration (quick runs of the bench's own code paths)
     "tiny": (64, 256, 4096,
              "tiny correctness case, N=64, D=256, V=4096, bias~N(0,0.1^2), 4 ignored rows, grad_logp=1"),
@@ -72,11 +76,11 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by sources_sha).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "e06004c466bb7265",
+    "sources_sha": "b71327e2ca00fe33",
     "how": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch per kernel (ncu -k one kernel, -c 1, "
             "1 pass), full-size workload, one box; box-to-box spread for the same build is large"),
-    "bytes_per_launch": {"fwd_partials": 2952650240 + 36931072, "dlogits": 5211738368 + 4280860416,
-                         "grad_hidden": 23447700992 + 697505792, "grad_weight": 11419964160 + 700668160},
+    "bytes_per_launch": {"fwd_partials": 1541312000 + 37103616, "dlogits": 2511923000 + 4270802000,
+                         "grad_hidden": 18679381000 + 699817216, "grad_weight": 11418937000 + 701517824},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
@@ -203,7 +207,7 @@ def oracle_sample_seconds(inp, rows: int) -> float:
 def make_workload(name):
     import workloads
     N, D, V, desc = WORKLOADS[name]
-    if name == "nemotron_n32":
+    if name in ("nemotron_n32", "nemotron_n16"):
         inp = workloads.nemotron_head(N=N, seed=1001)
     elif name == "tiny":
         inp = workloads.tiny()
@@ -245,6 +249,8 @@ def kernel_model(name, N, D, V, has_bias, has_tau):
         return 0.0, 4.0 * nseg_n * V * D + W
     if name == "bias_sum":
         return 0.0, 4.0 * V * (-(-N // 32)) + 4.0 * V
+    if name == "replicate_hidden":  # one read, eight copies written
+        return 0.0, H + 8.0 * H
     return 0.0, 0.0
 
 
@@ -336,7 +342,7 @@ def run_ours(args):
         raise RuntimeError("a kernel gave up on a bounded wait during warm-up")
     barrier()
 
-    cap = args.steps * 8
+    cap = args.steps * 12  # at most 9 launches per fwd+bwd step
     stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:

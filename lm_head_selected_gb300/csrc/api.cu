@@ -168,23 +168,27 @@ struct Carver {
 };
 
 struct FwdLayout {
-  size_t part_m, part_s, zt, total;
+  size_t part_m, part_s, zt, hrep, total;
+  int h_replicas;  // copies of the hidden states at hrep (1: none, the caller's array is read)
 };
 
-FwdLayout fwd_layout(int64_t N, int64_t V) {
+FwdLayout fwd_layout(int64_t N, int64_t D, int64_t V) {
   const size_t S = static_cast<size_t>(cdiv(V, llp::kSplitWidth));
   Carver c;
   FwdLayout L;
   L.part_m = c.take(S * N * sizeof(float));
   L.part_s = c.take(S * N * sizeof(float));
   L.zt = c.take(N * sizeof(float));
+  L.h_replicas = llp::hidden_replicas(N, D);
+  L.hrep = L.h_replicas > 1 ? c.take(static_cast<size_t>(L.h_replicas) * N * D * 2) : 0;
   L.total = c.off;
   return L;
 }
 
 struct BwdLayout {
-  size_t sched, dz, gb_part, dh_part, dw_part, total;
+  size_t sched, dz, gb_part, dh_part, dw_part, hrep, total;
   bool has_gb, has_dh, has_dw;
+  int h_replicas;
 };
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, bool want_dw) {
@@ -194,6 +198,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, b
   const size_t nseg_n = static_cast<size_t>(cdiv(N, llp::kKSegment));
   Carver c;
   BwdLayout L;
+  L.h_replicas = llp::hidden_replicas(N, D);
+  L.hrep = L.h_replicas > 1 ? c.take(static_cast<size_t>(L.h_replicas) * N * D * 2) : 0;
   L.sched = c.take(llp::kNumSchedCounters * sizeof(int));
   L.dz = c.take(static_cast<size_t>(N) * V_pad * 2);
   L.has_gb = bias;
@@ -273,12 +279,14 @@ enum KernelId {
   kKSegSumHidden,
   kKSegSumWeight,
   kKBiasSum,
+  kKReplicateHidden,
   kKNumKernels
 };
 
 const char* const kKernelNames[kKNumKernels] = {"fwd_partials",  "fwd_merge",          "dlogits",
                                                 "grad_hidden",   "grad_weight",        "segment_sum_hidden",
-                                                "segment_sum_weight", "bias_sum"};
+                                                "segment_sum_weight", "bias_sum",
+                                                "replicate_hidden"};
 
 struct Recorder {
   std::mutex mu;
@@ -328,6 +336,38 @@ RowTiling row_tiling(int64_t N) {
 // in flight while the MMAs read the other.
 int k_blocks_per_stage(int64_t D, bool single) { return ((LLP_KPS2 & 1) && !single && (D % 64) == 0) ? 2 : 1; }
 
+// 3-D map of R copies of a K-major [rows][cols] matrix laid end to end:
+// {cols, rows, R} with a 64-wide K box of box_rows rows in one copy.
+int make_map_replicas(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, int R, uint32_t box_rows,
+                      bool f16) {
+  cuuint64_t dims[3] = {cols, rows, static_cast<cuuint64_t>(R)};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(llp::kTileK), box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
+  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
+}
+
+// 4-D form of make_map_chunked over R copies laid end to end:
+// {64, rows, cols / 64, R}, a box taking one copy.
+int make_map_chunked_replicas(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, int R,
+                              uint32_t box_rows, uint32_t box_chunks, bool f16) {
+  cuuint64_t dims[4] = {64, rows, cols / 64, static_cast<cuuint64_t>(R)};
+  cuuint64_t strides[3] = {cols * 2, 128, cols * rows * 2};
+  cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
+  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
+}
+
 // Tensor maps of the two K-major operands of the forward / dlogits GEMMs, the
 // hidden states (box rows kTileM) and the weight (box rows w_box_rows): 2-D with
 // a 64-wide K box, or, with kps == 2, 3-D over 64-column K chunks, two chunks per box.
@@ -341,6 +381,15 @@ int make_kmajor_maps(CUtensorMap* tm_h, CUtensorMap* tm_w, const void* hidden, c
   return make_map(tm_w, weight, D, V, D * 2, llp::kTileK, w_box_rows, f16);
 }
 
+// Writes R copies of the hidden states [N][D] to dst (a workspace region) and
+// points tm_h at them: a 3-D K-major map whose third coordinate picks the copy.
+int replicate_hidden(DeviceInit* dev, const void* hidden, int64_t N, int64_t D, int R, uint8_t* dst, bool f16,
+                     CUtensorMap* tm_h, cudaStream_t s) {
+  if (llp::launch_replicate(hidden, static_cast<size_t>(N) * D * 2, R, dst, dev->num_sms, s) != cudaSuccess)
+    return fail_cuda(__LINE__);
+  return make_map_replicas(tm_h, dst, D, N, R, llp::kTileM, f16);
+}
+
 // Forward launch sequence on validated arguments (N > 0, workspace sized by fwd_layout).
 // With sh_max set, `weight` is a vocab shard whose row 0 is global id vocab_start,
 // and the shard's (max, sum, target logit) triple is written instead of logp / lse.
@@ -348,12 +397,18 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
              const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index, float* out_logp,
              float* out_lse, uint8_t* ws, cudaStream_t s, int64_t vocab_start = 0, float* sh_max = nullptr,
              float* sh_se = nullptr, float* sh_tl = nullptr, bool f16 = false) {
-  const FwdLayout L = fwd_layout(N, V);
+  const FwdLayout L = fwd_layout(N, D, V);
   const RowTiling T = row_tiling(N);
   CUtensorMap tm_h, tm_w;
   const int kps = k_blocks_per_stage(D, T.single);
   if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16) != LLP_OK)
     return fail_cuda(__LINE__);
+  rec_mark(s, -1);
+  const int h_reps = T.single && kps == 1 ? L.h_replicas : 1;
+  if (h_reps > 1) {
+    if (replicate_hidden(dev, hidden, N, D, h_reps, ws + L.hrep, f16, &tm_h, s) != LLP_OK) return fail_cuda(__LINE__);
+    rec_mark(s, kKReplicateHidden);
+  }
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
@@ -374,8 +429,8 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.global_V = V;
   p.f16 = f16 ? 1 : 0;
   p.kps = kps;
+  p.h_replicas = h_reps;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
-  rec_mark(s, -1);
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s, T.single) != cudaSuccess) return fail_cuda(__LINE__);
   rec_mark(s, kKFwdPartials);
   if (sh_max != nullptr) {
@@ -435,11 +490,19 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
 
   // B1: dlogits (+ grad_bias partials)
   const RowTiling T = row_tiling(N);
+  // copies of a small batch's hidden states, read by dlogits and grad_weight
+  const bool h_rep = L.h_replicas > 1 && T.single && k_blocks_per_stage(D, T.single) == 1;
   {
     CUtensorMap tm_h, tm_w;
     const int kps = k_blocks_per_stage(D, T.single);
     if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16) != LLP_OK)
       return fail_cuda(__LINE__);
+    rec_mark(s, -1);
+    if (h_rep) {
+      if (replicate_hidden(dev, hidden, N, D, L.h_replicas, ws + L.hrep, f16, &tm_h, s) != LLP_OK)
+        return fail_cuda(__LINE__);
+      rec_mark(s, kKReplicateHidden);
+    }
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -462,8 +525,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.sched_reset = sched;
     p.f16 = f16 ? 1 : 0;
     p.kps = kps;
+    p.h_replicas = h_rep ? L.h_replicas : 1;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
-    rec_mark(s, -1);
     // dz [N][V_pad], written in 64 x 32 slabs; the columns [V, V_pad) of the last
     // slab are zeros, so readers may treat every row as V_pad long
     CUtensorMap tm_dz_out;
@@ -525,6 +588,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       p.a_chunked = 0;
       p.b_chunked = w_chunked ? 1 : 0;
       p.kps = kps;
+      p.h_replicas = 1;
       p.rows = static_cast<int>(N);
       p.D = static_cast<int>(D);
       p.K = static_cast<int>(V);
@@ -574,7 +638,12 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     } else if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) {
       return fail_cuda(__LINE__);
     }
-    if (h_chunked) {
+    const int gw_reps = h_rep && h_chunked && kps == 1 ? L.h_replicas : 1;
+    if (gw_reps > 1) {
+      if (make_map_chunked_replicas(&tm_h_mn, ws + L.hrep, D, N, gw_reps, llp::kTileK, llp::kBRows / 64, f16) !=
+          LLP_OK)
+        return fail_cuda(__LINE__);
+    } else if (h_chunked) {
       if (make_map_chunked(&tm_h_mn, hidden, D, N, D * 2, llp::kTileK * kps, llp::kBRows / 64, f16) != LLP_OK)
         return fail_cuda(__LINE__);
     } else if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) {
@@ -584,6 +653,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.a_chunked = dz_chunked ? 1 : 0;
     p.b_chunked = h_chunked ? 1 : 0;
     p.kps = kps;
+    p.h_replicas = gw_reps;
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
     p.K = static_cast<int>(N);
@@ -633,7 +703,7 @@ extern "C" {
 
 size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V) {
   if (N <= 0 || check_shapes(N, D, V) != LLP_OK) return 0;
-  return fwd_layout(N, V).total;
+  return fwd_layout(N, D, V).total;
 }
 
 size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_bias) {
@@ -668,7 +738,7 @@ static int fwd_entry(const void* hidden, const void* weight, const float* bias, 
   if (st != LLP_OK) return st;
   if (out_logp == nullptr || out_lse == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(out_logp, 4) || !aligned(out_lse, 4)) return LLP_ERR_MISALIGNED;
-  const FwdLayout L = fwd_layout(N, V);
+  const FwdLayout L = fwd_layout(N, D, V);
   if (workspace == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
   if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
@@ -773,7 +843,9 @@ static IdxLayout idx_layout(int64_t N, int64_t D, int64_t V, int64_t K, bool bwd
   L.c_a = c.take(Kc * 4);  // forward: compact logp; backward: compact grad_logp
   L.c_b = c.take(Kc * 4);  // compact lse
   L.c_gh = bwd ? c.take(Kc * D * 2) : 0;
-  L.inner = c.take(L.Kc > 0 ? (bwd ? bwd_layout(L.Kc, D, V, bias, true, true).total : fwd_layout(L.Kc, V).total) : 0);
+  L.inner = c.take(L.Kc > 0 ? (bwd ? bwd_layout(L.Kc, D, V, bias, true, true).total
+                                   : fwd_layout(L.Kc, D, V).total)
+                            : 0);
   L.total = c.off;
   return L;
 }
@@ -941,7 +1013,7 @@ static int fwd_shard_entry(const void* hidden, const void* weight_local, const f
     return LLP_ERR_NULL_POINTER;
   if (!aligned(out_max, 4) || !aligned(out_sumexp, 4) || !aligned(out_target_logit, 4) || !aligned(workspace, 16))
     return LLP_ERR_MISALIGNED;
-  if (workspace_bytes < fwd_layout(N, V_local).total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < fwd_layout(N, D, V_local).total) return LLP_ERR_WORKSPACE_TOO_SMALL;
   DeviceInit* dev = nullptr;
   if ((st = init_device(&dev)) != LLP_OK) return st;
   if ((st = load_encode_fn()) != LLP_OK) return st;
@@ -1298,7 +1370,7 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   if (st != LLP_OK) return st;
   if (out_logp == nullptr || out_lse == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(out_logp, 4) || !aligned(out_lse, 4)) return LLP_ERR_MISALIGNED;
-  const FwdLayout L = fwd_layout(N, V);
+  const FwdLayout L = fwd_layout(N, D, V);
   if (L.total > static_cast<size_t>(LINEAR_LOGP_NOALLOC_SCRATCH_BYTES)) return LLP_ERR_SCRATCH_LIMIT;
 
   DeviceInit* dev = nullptr;

@@ -96,6 +96,20 @@ cudaError_t small_grad_hidden_setup();
 cudaError_t launch_small_grad_hidden(const CUtensorMap& tm_w, const CUtensorMap& tm_dz, const GhSmallParams& p,
                                      int num_sms, cudaStream_t s);
 
+#ifndef LLP_H_REPLICA_MAX_N
+#define LLP_H_REPLICA_MAX_N 24   // batches of at most this many rows read per-CTA copies of the hidden states (0: off)
+#endif
+// Copies of a small batch's hidden states: every CTA of the forward / dlogits
+// (and every pair of grad_weight) re-reads all of them, and a single copy sits
+// in a few L2 slices that then serve the whole launch.
+constexpr int kHReplicas = 8;
+constexpr long long kHReplicaMaxBytes = 4ll << 20;  // all copies together
+inline int hidden_replicas(long long N, long long D) {
+  return (N <= LLP_H_REPLICA_MAX_N && kHReplicas * N * D * 2 <= kHReplicaMaxBytes) ? kHReplicas : 1;
+}
+// dst = R consecutive copies of the `bytes` bytes at src (16-byte multiples, 16-byte aligned).
+cudaError_t launch_replicate(const void* src, size_t bytes, int R, void* dst, int num_sms, cudaStream_t s);
+
 // Resident work groups (CTA pairs, or CTAs in single mode) per GEMM kernel,
 // found once per device; the persistent grids never exceed them.
 struct LaunchCaps {
@@ -122,6 +136,7 @@ struct FwdParams {
   long long global_V;     // global vocab size (== V unless sharded)
   int f16;                // hidden / weight are IEEE fp16 (else bf16)
   int kps;                // k-blocks per pipeline stage: 2 with 3-D chunked maps (D % 64 == 0), else 1
+  int h_replicas;         // > 1: the hidden map's third dimension selects a copy (single-CTA tiles only)
 };
 
 struct DzParams {
@@ -141,6 +156,7 @@ struct DzParams {
   int* sched_reset;       // [kNumSchedCounters] ticket counters of the gradient GEMMs, zeroed at launch
   int f16;                // hidden / weight / dz are IEEE fp16 (else bf16)
   int kps;                // k-blocks per pipeline stage: 2 with 3-D chunked maps (D % 64 == 0), else 1
+  int h_replicas;         // > 1: the hidden map's third dimension selects a copy (single-CTA tiles only)
 };
 
 // Ticket counters of the in-order scheduled gradient GEMMs (one per GEMM of a
@@ -161,6 +177,7 @@ struct GradGemmParams {
   unsigned int* progress;  // k-blocks issued by all pairs, 0 at launch (advisory lockstep); nullptr: off
   int a_chunked, b_chunked;  // the MN-major operand's map is 3-D {64, K, MN/64}: one copy per stage
   int kps;             // k-blocks per pipeline stage: 2 when every operand map is 3-D, else 1
+  int h_replicas;      // grad_weight: > 1, the chunked hidden map's fourth dimension selects a copy
   int f16;             // operands and the 16-bit output are IEEE fp16 (else bf16)
 };
 
