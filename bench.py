@@ -50,7 +50,7 @@ WORKLOADS = {
     "nemotron_n32": (32, 2688, 131072,
                      "Nemotron-3-Nano LM head, N=32 (2x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
                      "uniform targets, grad_logp=1"),
-    # batch 1 x seq 16 on the same head: the GEMMs read per-CTA copies of the hidden states
+    # batch 1 x seq 16 on the same head: grad_weight reads per-pair copies of the hidden states
     "nemotron_n16": (16, 2688, 131072,
                      "Nemotron-3-Nano LM head, N=16 (1x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
                      "uniform targets, grad_logp=1"),
@@ -76,11 +76,11 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by sources_sha).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "b71327e2ca00fe33",
+    "sources_sha": "fbaaeefeefae5f32",
     "how": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch per kernel (ncu -k one kernel, -c 1, "
             "1 pass), full-size workload, one box; box-to-box spread for the same build is large"),
-    "bytes_per_launch": {"fwd_partials": 1541312000 + 37103616, "dlogits": 2511923000 + 4270802000,
-                         "grad_hidden": 18679381000 + 699817216, "grad_weight": 11418937000 + 701517824},
+    "bytes_per_launch": {"fwd_partials": 1552126000 + 37303296, "dlogits": 2535230000 + 4271106000,
+                         "grad_hidden": 22358892000 + 699863808, "grad_weight": 11420964000 + 700686336},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")

@@ -88,16 +88,14 @@ enum {
  * batches through the two-CTA GEMM too (a diagnostic, read once per process).
  *
  * Small-batch note: for a batch of at most 24 rows (and 8 x N x D x 2 bytes of
- * at most 4 MiB) the forward and the backward each first copy the hidden
- * states eight times into their workspace, and the GEMMs that every SM runs
- * over the same hidden rows (forward, dlogits, grad_weight) spread their reads
- * over those copies.  A copy is bit for bit the caller's array, so the results
- * do not change. */
+ * at most 4 MiB, D a multiple of 64) the backward copies the hidden states
+ * eight times into its workspace before grad_weight, whose CTA pairs all read
+ * the same hidden rows at nearly the same time, and each pair reads one copy.
+ * A copy is bit for bit the caller's array, so the results do not change. */
 
 /* Bytes of workspace linear_logp_fwd needs for an N x D x V problem
- * (0 when N == 0).  The workspace holds the per-vocab-split (max, sum) pairs,
- * the captured target logits and, for a small batch, the copies of the hidden
- * states. */
+ * (0 when N == 0).  The workspace holds the per-vocab-split (max, sum) pairs
+ * and the captured target logits. */
 size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V);
 
 /* Bytes of workspace linear_logp_bwd needs: two work-ticket counters of the

@@ -168,19 +168,16 @@ struct Carver {
 };
 
 struct FwdLayout {
-  size_t part_m, part_s, zt, hrep, total;
-  int h_replicas;  // copies of the hidden states at hrep (1: none, the caller's array is read)
+  size_t part_m, part_s, zt, total;
 };
 
-FwdLayout fwd_layout(int64_t N, int64_t D, int64_t V) {
+FwdLayout fwd_layout(int64_t N, int64_t V) {
   const size_t S = static_cast<size_t>(cdiv(V, llp::kSplitWidth));
   Carver c;
   FwdLayout L;
   L.part_m = c.take(S * N * sizeof(float));
   L.part_s = c.take(S * N * sizeof(float));
   L.zt = c.take(N * sizeof(float));
-  L.h_replicas = llp::hidden_replicas(N, D);
-  L.hrep = L.h_replicas > 1 ? c.take(static_cast<size_t>(L.h_replicas) * N * D * 2) : 0;
   L.total = c.off;
   return L;
 }
@@ -188,7 +185,7 @@ FwdLayout fwd_layout(int64_t N, int64_t D, int64_t V) {
 struct BwdLayout {
   size_t sched, dz, gb_part, dh_part, dw_part, hrep, total;
   bool has_gb, has_dh, has_dw;
-  int h_replicas;
+  int h_replicas;  // copies of the hidden states at hrep for grad_weight (1: none)
 };
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, bool want_dw) {
@@ -198,7 +195,7 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, b
   const size_t nseg_n = static_cast<size_t>(cdiv(N, llp::kKSegment));
   Carver c;
   BwdLayout L;
-  L.h_replicas = llp::hidden_replicas(N, D);
+  L.h_replicas = want_dw ? llp::hidden_replicas(N, D) : 1;
   L.hrep = L.h_replicas > 1 ? c.take(static_cast<size_t>(L.h_replicas) * N * D * 2) : 0;
   L.sched = c.take(llp::kNumSchedCounters * sizeof(int));
   L.dz = c.take(static_cast<size_t>(N) * V_pad * 2);
@@ -332,25 +329,10 @@ RowTiling row_tiling(int64_t N) {
 // K-blocks per pipeline stage of the forward / dlogits GEMMs: two (one 3-D copy
 // per operand per stage) on CTA pairs when the hidden size is whole 64-column
 // chunks.  The single-CTA tiling of small batches streams the weight from HBM
-// and keeps its four one-k-block stages: two double-size stages leave only one
-// in flight while the MMAs read the other.
+// and keeps one-k-block stages: with 128-row hidden boxes two double stages
+// would leave only one in flight while the MMAs read the other, and with
+// 32-row boxes three double stages ran no faster than six single ones.
 int k_blocks_per_stage(int64_t D, bool single) { return ((LLP_KPS2 & 1) && !single && (D % 64) == 0) ? 2 : 1; }
-
-// 3-D map of R copies of a K-major [rows][cols] matrix laid end to end:
-// {cols, rows, R} with a 64-wide K box of box_rows rows in one copy.
-int make_map_replicas(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, int R, uint32_t box_rows,
-                      bool f16) {
-  cuuint64_t dims[3] = {cols, rows, static_cast<cuuint64_t>(R)};
-  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(llp::kTileK), box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
-  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
-}
 
 // 4-D form of make_map_chunked over R copies laid end to end:
 // {64, rows, cols / 64, R}, a box taking one copy.
@@ -372,22 +354,13 @@ int make_map_chunked_replicas(CUtensorMap* m, const void* base, uint64_t cols, u
 // hidden states (box rows kTileM) and the weight (box rows w_box_rows): 2-D with
 // a 64-wide K box, or, with kps == 2, 3-D over 64-column K chunks, two chunks per box.
 int make_kmajor_maps(CUtensorMap* tm_h, CUtensorMap* tm_w, const void* hidden, const void* weight, int64_t N,
-                     int64_t D, int64_t V, int w_box_rows, int kps, bool f16) {
+                     int64_t D, int64_t V, int w_box_rows, int kps, bool f16, int h_box_rows = llp::kTileM) {
   if (kps == 2) {
-    if (make_map_chunked(tm_h, hidden, D, N, D * 2, llp::kTileM, 2, f16) != LLP_OK) return LLP_ERR_CUDA;
+    if (make_map_chunked(tm_h, hidden, D, N, D * 2, h_box_rows, 2, f16) != LLP_OK) return LLP_ERR_CUDA;
     return make_map_chunked(tm_w, weight, D, V, D * 2, w_box_rows, 2, f16);
   }
-  if (make_map(tm_h, hidden, D, N, D * 2, llp::kTileK, llp::kTileM, f16) != LLP_OK) return LLP_ERR_CUDA;
+  if (make_map(tm_h, hidden, D, N, D * 2, llp::kTileK, h_box_rows, f16) != LLP_OK) return LLP_ERR_CUDA;
   return make_map(tm_w, weight, D, V, D * 2, llp::kTileK, w_box_rows, f16);
-}
-
-// Writes R copies of the hidden states [N][D] to dst (a workspace region) and
-// points tm_h at them: a 3-D K-major map whose third coordinate picks the copy.
-int replicate_hidden(DeviceInit* dev, const void* hidden, int64_t N, int64_t D, int R, uint8_t* dst, bool f16,
-                     CUtensorMap* tm_h, cudaStream_t s) {
-  if (llp::launch_replicate(hidden, static_cast<size_t>(N) * D * 2, R, dst, dev->num_sms, s) != cudaSuccess)
-    return fail_cuda(__LINE__);
-  return make_map_replicas(tm_h, dst, D, N, R, llp::kTileM, f16);
 }
 
 // Forward launch sequence on validated arguments (N > 0, workspace sized by fwd_layout).
@@ -397,18 +370,13 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
              const float* temperature, int64_t N, int64_t D, int64_t V, int64_t ignore_index, float* out_logp,
              float* out_lse, uint8_t* ws, cudaStream_t s, int64_t vocab_start = 0, float* sh_max = nullptr,
              float* sh_se = nullptr, float* sh_tl = nullptr, bool f16 = false) {
-  const FwdLayout L = fwd_layout(N, D, V);
+  const FwdLayout L = fwd_layout(N, V);
   const RowTiling T = row_tiling(N);
   CUtensorMap tm_h, tm_w;
   const int kps = k_blocks_per_stage(D, T.single);
-  if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16) != LLP_OK)
+  if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16,
+                       llp::hidden_box_rows(N, T.single)) != LLP_OK)
     return fail_cuda(__LINE__);
-  rec_mark(s, -1);
-  const int h_reps = T.single && kps == 1 ? L.h_replicas : 1;
-  if (h_reps > 1) {
-    if (replicate_hidden(dev, hidden, N, D, h_reps, ws + L.hrep, f16, &tm_h, s) != LLP_OK) return fail_cuda(__LINE__);
-    rec_mark(s, kKReplicateHidden);
-  }
   llp::FwdParams p;
   p.N = static_cast<int>(N);
   p.D = static_cast<int>(D);
@@ -429,8 +397,8 @@ int fwd_core(DeviceInit* dev, const void* hidden, const void* weight, const floa
   p.global_V = V;
   p.f16 = f16 ? 1 : 0;
   p.kps = kps;
-  p.h_replicas = h_reps;
   const int64_t units = static_cast<int64_t>(p.num_m) * p.num_splits;
+  rec_mark(s, -1);
   if (llp::launch_fwd_partials(tm_h, tm_w, p, units, dev->caps, s, T.single) != cudaSuccess) return fail_cuda(__LINE__);
   rec_mark(s, kKFwdPartials);
   if (sh_max != nullptr) {
@@ -490,19 +458,12 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
 
   // B1: dlogits (+ grad_bias partials)
   const RowTiling T = row_tiling(N);
-  // copies of a small batch's hidden states, read by dlogits and grad_weight
-  const bool h_rep = L.h_replicas > 1 && T.single && k_blocks_per_stage(D, T.single) == 1;
   {
     CUtensorMap tm_h, tm_w;
     const int kps = k_blocks_per_stage(D, T.single);
-    if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16) != LLP_OK)
+    if (make_kmajor_maps(&tm_h, &tm_w, hidden, weight, N, D, V, T.w_box_rows, kps, f16,
+                         llp::hidden_box_rows(N, T.single)) != LLP_OK)
       return fail_cuda(__LINE__);
-    rec_mark(s, -1);
-    if (h_rep) {
-      if (replicate_hidden(dev, hidden, N, D, L.h_replicas, ws + L.hrep, f16, &tm_h, s) != LLP_OK)
-        return fail_cuda(__LINE__);
-      rec_mark(s, kKReplicateHidden);
-    }
     llp::DzParams p;
     p.N = static_cast<int>(N);
     p.D = static_cast<int>(D);
@@ -525,8 +486,8 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.sched_reset = sched;
     p.f16 = f16 ? 1 : 0;
     p.kps = kps;
-    p.h_replicas = h_rep ? L.h_replicas : 1;
     const int64_t units = static_cast<int64_t>(p.num_m) * p.num_vt;
+    rec_mark(s, -1);
     // dz [N][V_pad], written in 64 x 32 slabs; the columns [V, V_pad) of the last
     // slab are zeros, so readers may treat every row as V_pad long
     CUtensorMap tm_dz_out;
@@ -638,8 +599,14 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     } else if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) {
       return fail_cuda(__LINE__);
     }
-    const int gw_reps = h_rep && h_chunked && kps == 1 ? L.h_replicas : 1;
+    // copies of a small batch's hidden states: every CTA pair reads all of
+    // them at nearly the same k-block, and one copy sits in a few L2 slices
+    const int gw_reps = L.h_replicas > 1 && h_chunked && kps == 1 ? L.h_replicas : 1;
     if (gw_reps > 1) {
+      if (llp::launch_replicate(hidden, static_cast<size_t>(N) * D * 2, gw_reps, ws + L.hrep, dev->num_sms, s) !=
+          cudaSuccess)
+        return fail_cuda(__LINE__);
+      rec_mark(s, kKReplicateHidden);
       if (make_map_chunked_replicas(&tm_h_mn, ws + L.hrep, D, N, gw_reps, llp::kTileK, llp::kBRows / 64, f16) !=
           LLP_OK)
         return fail_cuda(__LINE__);
@@ -703,7 +670,7 @@ extern "C" {
 
 size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V) {
   if (N <= 0 || check_shapes(N, D, V) != LLP_OK) return 0;
-  return fwd_layout(N, D, V).total;
+  return fwd_layout(N, V).total;
 }
 
 size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_bias) {
@@ -738,7 +705,7 @@ static int fwd_entry(const void* hidden, const void* weight, const float* bias, 
   if (st != LLP_OK) return st;
   if (out_logp == nullptr || out_lse == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(out_logp, 4) || !aligned(out_lse, 4)) return LLP_ERR_MISALIGNED;
-  const FwdLayout L = fwd_layout(N, D, V);
+  const FwdLayout L = fwd_layout(N, V);
   if (workspace == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(workspace, 16)) return LLP_ERR_MISALIGNED;
   if (workspace_bytes < L.total) return LLP_ERR_WORKSPACE_TOO_SMALL;
@@ -844,7 +811,7 @@ static IdxLayout idx_layout(int64_t N, int64_t D, int64_t V, int64_t K, bool bwd
   L.c_b = c.take(Kc * 4);  // compact lse
   L.c_gh = bwd ? c.take(Kc * D * 2) : 0;
   L.inner = c.take(L.Kc > 0 ? (bwd ? bwd_layout(L.Kc, D, V, bias, true, true).total
-                                   : fwd_layout(L.Kc, D, V).total)
+                                   : fwd_layout(L.Kc, V).total)
                             : 0);
   L.total = c.off;
   return L;
@@ -1013,7 +980,7 @@ static int fwd_shard_entry(const void* hidden, const void* weight_local, const f
     return LLP_ERR_NULL_POINTER;
   if (!aligned(out_max, 4) || !aligned(out_sumexp, 4) || !aligned(out_target_logit, 4) || !aligned(workspace, 16))
     return LLP_ERR_MISALIGNED;
-  if (workspace_bytes < fwd_layout(N, D, V_local).total) return LLP_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < fwd_layout(N, V_local).total) return LLP_ERR_WORKSPACE_TOO_SMALL;
   DeviceInit* dev = nullptr;
   if ((st = init_device(&dev)) != LLP_OK) return st;
   if ((st = load_encode_fn()) != LLP_OK) return st;
@@ -1370,7 +1337,7 @@ int linear_logp_fwd_noalloc(const void* hidden, const void* weight, const float*
   if (st != LLP_OK) return st;
   if (out_logp == nullptr || out_lse == nullptr) return LLP_ERR_NULL_POINTER;
   if (!aligned(out_logp, 4) || !aligned(out_lse, 4)) return LLP_ERR_MISALIGNED;
-  const FwdLayout L = fwd_layout(N, D, V);
+  const FwdLayout L = fwd_layout(N, V);
   if (L.total > static_cast<size_t>(LINEAR_LOGP_NOALLOC_SCRATCH_BYTES)) return LLP_ERR_SCRATCH_LIMIT;
 
   DeviceInit* dev = nullptr;

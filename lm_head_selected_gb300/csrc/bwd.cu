@@ -67,13 +67,15 @@ __device__ __forceinline__ uint32_t pack16x2(bool f16, float a, float b) {
 // B1: dlogits
 // ----------------------------------------------------------------------------
 // PAIRED = false: single CTAs with 128-row tiles, for a batch that fits in one.
-template <bool HAS_BIAS, bool PAIRED = kPairMMA>
+// AROWS: hidden rows loaded per stage (kSmallARows for a batch that small).
+template <bool HAS_BIAS, bool PAIRED = kPairMMA, int AROWS = kTileM>
 struct DzCfg {
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
   static constexpr bool PAIR = PAIRED;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = PAIR ? kPairStages : 4;
+  static constexpr int A_ROWS = AROWS;
+  static constexpr int STAGES = PAIR ? kPairStages : (AROWS < kTileM ? kSmallADzStages : 4);
   static constexpr int EXTRA_SMEM = kEpiSmemBytes;
   static constexpr int UM = PAIR ? kUnitM : kTileM;
   using Params = DzParams;
@@ -93,7 +95,6 @@ struct DzCfg {
   static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
   static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
   static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
-  static __device__ __forceinline__ int a_replicas(const Params& p) { return p.h_replicas; }
   static __device__ __forceinline__ int b_replicas(const Params&) { return 1; }
   // the gradient GEMMs that follow on the stream start from ticket 0
   static __device__ __forceinline__ void on_launch(const Params& p) {
@@ -223,6 +224,7 @@ struct GradCfg {
   static_assert(B_MN, "half-width column tiles load B in 64-row MN-major boxes");
   static constexpr bool PAIR = kPairMMA;
   static constexpr int BN = kTileN;
+  static constexpr int A_ROWS = BM;
   static constexpr int STAGES = PAIR ? kPairStages : 4;
   static constexpr int EXTRA_SMEM = kEpiSmemBytes;
   static constexpr int UM = kUnitM;
@@ -243,7 +245,6 @@ struct GradCfg {
   static __device__ __forceinline__ bool b_chunked(const Params& p) { return p.b_chunked != 0; }
   static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
   // grad_weight's B is the hidden states
-  static __device__ __forceinline__ int a_replicas(const Params&) { return 1; }
   static __device__ __forceinline__ int b_replicas(const Params& p) { return A_MN ? p.h_replicas : 1; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
@@ -388,12 +389,18 @@ cudaError_t bwd_setup(LaunchCaps* caps) {
   if ((e = setup_gemm<DzCfg<true>>(&caps->dz_groups[1])) != cudaSuccess) return e;
   if ((e = setup_gemm<DzCfg<false, false>>(&caps->dz_single[0])) != cudaSuccess) return e;
   if ((e = setup_gemm<DzCfg<true, false>>(&caps->dz_single[1])) != cudaSuccess) return e;
+  if ((e = setup_gemm<DzCfg<false, false, kSmallARows>>(&caps->dz_small[0])) != cudaSuccess) return e;
+  if ((e = setup_gemm<DzCfg<true, false, kSmallARows>>(&caps->dz_small[1])) != cudaSuccess) return e;
   if ((e = setup_gemm<GradCfg<false, true>>(&caps->gh_groups)) != cudaSuccess) return e;
   return setup_gemm<GradCfg<true, true>>(&caps->gw_groups);
 }
 
 cudaError_t launch_dlogits(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_dz_out,
                            const DzParams& p, long long units, const LaunchCaps& caps, cudaStream_t s, bool single) {
+  if (single && hidden_box_rows(p.N, true) == kSmallARows)
+    return p.bias ? launch_units<DzCfg<true, false, kSmallARows>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_small[1], s)
+                  : launch_units<DzCfg<false, false, kSmallARows>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_small[0],
+                                                                   s);
   if (single)
     return p.bias ? launch_units<DzCfg<true, false>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_single[1], s)
                   : launch_units<DzCfg<false, false>>(tm_h, tm_w, tm_dz_out, p, units, caps.dz_single[0], s);

@@ -29,14 +29,16 @@ __device__ __forceinline__ bool target_valid(long long t, int V, long long ignor
 }
 
 // PAIRED = false: single CTAs with 128-row tiles, used when the whole batch fits
-// in one of them (a pair's second CTA would hold only padding rows).
-template <bool HAS_BIAS, bool PAIRED = kPairMMA>
+// in one of them (a pair's second CTA would hold only padding rows).  AROWS:
+// hidden rows loaded per stage (kSmallARows for a batch that small).
+template <bool HAS_BIAS, bool PAIRED = kPairMMA, int AROWS = kTileM>
 struct FwdCfg {
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
   static constexpr bool PAIR = PAIRED;
   static constexpr int BN = kTileN;
-  static constexpr int STAGES = PAIR ? kPairStages : 4;
+  static constexpr int A_ROWS = AROWS;
+  static constexpr int STAGES = PAIR ? kPairStages : (AROWS < kTileM ? kSmallAFwdStages : 4);
   static constexpr int EXTRA_SMEM = 0;
   static constexpr int TPS = kTilesPerSplit;
   static constexpr int UM = PAIR ? kUnitM : kTileM;
@@ -59,7 +61,6 @@ struct FwdCfg {
   static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
   static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
   static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
-  static __device__ __forceinline__ int a_replicas(const Params& p) { return p.h_replicas; }
   static __device__ __forceinline__ int b_replicas(const Params&) { return 1; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
@@ -333,6 +334,8 @@ cudaError_t fwd_setup(LaunchCaps* caps) {
   if (e == cudaSuccess) e = setup_gemm<FwdCfg<true>>(&caps->fwd_groups[1]);
   if (e == cudaSuccess) e = setup_gemm<FwdCfg<false, false>>(&caps->fwd_single[0]);
   if (e == cudaSuccess) e = setup_gemm<FwdCfg<true, false>>(&caps->fwd_single[1]);
+  if (e == cudaSuccess) e = setup_gemm<FwdCfg<false, false, kSmallARows>>(&caps->fwd_small[0]);
+  if (e == cudaSuccess) e = setup_gemm<FwdCfg<true, false, kSmallARows>>(&caps->fwd_small[1]);
   return e;
 }
 
@@ -345,6 +348,9 @@ static cudaError_t launch_units(const CUtensorMap& a, const CUtensorMap& b, cons
 
 cudaError_t launch_fwd_partials(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdParams& p,
                                 long long units, const LaunchCaps& caps, cudaStream_t s, bool single) {
+  if (single && hidden_box_rows(p.N, true) == kSmallARows)
+    return p.bias ? launch_units<FwdCfg<true, false, kSmallARows>>(tm_h, tm_w, p, units, caps.fwd_small[1], s)
+                  : launch_units<FwdCfg<false, false, kSmallARows>>(tm_h, tm_w, p, units, caps.fwd_small[0], s);
   if (single)
     return p.bias ? launch_units<FwdCfg<true, false>>(tm_h, tm_w, p, units, caps.fwd_single[1], s)
                   : launch_units<FwdCfg<false, false>>(tm_h, tm_w, p, units, caps.fwd_single[0], s);

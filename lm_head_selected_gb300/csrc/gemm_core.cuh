@@ -81,7 +81,9 @@ struct Plan {
   static constexpr int NCTA = PAIR ? 2 : 1;
   static constexpr int UM = NCTA * BM;                         // unit rows (M) per tile
   static constexpr int B_ROWS = PAIR ? Cfg::BN / 2 : Cfg::BN;  // B rows each CTA loads
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_BYTES = Cfg::A_ROWS * BK * 2;  // A rows loaded per k-block (the MMA reads BM)
+  static_assert(Cfg::A_ROWS == BM || (!PAIR && !Cfg::A_MN && A_BYTES + Cfg::BN * BK * 2 >= BM * BK * 2),
+                "short A boxes: single CTA, K-major A, and the MMA's BM rows must stay inside the stage");
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = NCTA * STAGE_BYTES;  // bytes landing per stage on the MMA's barrier
@@ -258,10 +260,9 @@ __device__ __forceinline__ void run_producer_k(const SharedState& st, const CUte
   // decides anything about the arithmetic.
   unsigned int* const prog = dyn && leader ? Cfg::progress_counter(p) : nullptr;
   const unsigned int npairs = gridDim.x / P::NCTA;
-  // Copies of an operand that every CTA re-reads (the hidden states of a small
-  // batch): each CTA (pair) reads its own, so the few L2 slices that would
-  // hold a single copy do not serve the whole launch.
-  const int a_reps = Cfg::a_replicas(p);
+  // Copies of an operand that every CTA pair re-reads (grad_weight's hidden
+  // states of a small batch): each pair reads its own, so the few L2 slices
+  // that would hold a single copy do not serve the whole launch.
   const int b_reps = Cfg::b_replicas(p);
   unsigned int mine = 0;
   for (int k = 0;; ++k) {
@@ -337,8 +338,6 @@ __device__ __forceinline__ void run_producer_k(const SharedState& st, const CUte
           if (!Cfg::A_MN) {
             if (kps == 2)
               tma_load_3d(sA, tmA, &st.full[stage], 0, a_row, kx / 64, polA);
-            else if (a_reps > 1)  // this CTA's copy of a small, hot operand
-              tma_load_3d(sA, tmA, &st.full[stage], kx, a_row, static_cast<int>(blockIdx.x) % a_reps, polA);
             else
               tma_load_2d(sA, tmA, &st.full[stage], kx, a_row, polA);
           } else if (Cfg::a_chunked(p)) {
@@ -443,7 +442,7 @@ __device__ __forceinline__ void run_mma_k(const SharedState& st, const typename 
         for (int c = 0; c < kps; ++c) {
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t ad = ad0 + operand_offset<Cfg::A_MN>(c, kk, BM);
+            const uint64_t ad = ad0 + operand_offset<Cfg::A_MN>(c, kk, Cfg::A_ROWS);
             const uint64_t bd = bd0 + operand_offset<Cfg::B_MN>(c, kk, P::B_ROWS);
             const uint32_t acc = (kb > 0 || c > 0 || kk > 0) ? 1u : 0u;
             if (P::PAIR)

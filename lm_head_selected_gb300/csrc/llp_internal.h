@@ -96,12 +96,28 @@ cudaError_t small_grad_hidden_setup();
 cudaError_t launch_small_grad_hidden(const CUtensorMap& tm_w, const CUtensorMap& tm_dz, const GhSmallParams& p,
                                      int num_sms, cudaStream_t s);
 
-#ifndef LLP_H_REPLICA_MAX_N
-#define LLP_H_REPLICA_MAX_N 24   // batches of at most this many rows read per-CTA copies of the hidden states (0: off)
+#ifndef LLP_SMALL_A
+#define LLP_SMALL_A 1        // single-CTA forward / dlogits of <= kSmallARows rows load only those hidden rows
 #endif
-// Copies of a small batch's hidden states: every CTA of the forward / dlogits
-// (and every pair of grad_weight) re-reads all of them, and a single copy sits
-// in a few L2 slices that then serve the whole launch.
+// A batch of at most kSmallARows rows (single-CTA tiles) loads a kSmallARows-row
+// hidden box per stage instead of a kTileM-row one.  The MMA still reads kTileM
+// rows: the rest fall on the stage's weight tile and feed only accumulator rows
+// past the batch, which no epilogue writes.  The bytes saved hold more weight
+// stages, and the weight stream of these HBM-bound kernels goes faster.
+constexpr int kSmallARows = 32;
+constexpr int kSmallAFwdStages = 6;  // 6 x 36 KB
+constexpr int kSmallADzStages = 5;   // 5 x 36 KB + the epilogue's 32 KB of store buffers
+// Rows of the hidden-state box that the forward / dlogits maps use for N rows.
+inline int hidden_box_rows(long long N, bool single) {
+  return (LLP_SMALL_A && single && N <= kSmallARows) ? kSmallARows : kTileM;
+}
+
+#ifndef LLP_H_REPLICA_MAX_N
+#define LLP_H_REPLICA_MAX_N 24   // batches of at most this many rows give grad_weight per-pair hidden-state copies (0: off)
+#endif
+// Copies of a small batch's hidden states for grad_weight: every CTA pair
+// re-reads all of them at nearly the same k-block, and a single copy sits in a
+// few L2 slices that then serve the whole launch.
 constexpr int kHReplicas = 8;
 constexpr long long kHReplicaMaxBytes = 4ll << 20;  // all copies together
 inline int hidden_replicas(long long N, long long D) {
@@ -115,8 +131,10 @@ cudaError_t launch_replicate(const void* src, size_t bytes, int R, void* dst, in
 struct LaunchCaps {
   int fwd_groups[2];  // [has_bias]
   int fwd_single[2];  // [has_bias], single-CTA forward for batches of at most kTileM rows
+  int fwd_small[2];   // [has_bias], single-CTA forward with kSmallARows-row hidden boxes
   int dz_groups[2];   // [has_bias]
   int dz_single[2];   // [has_bias], single-CTA dlogits for batches of at most kTileM rows
+  int dz_small[2];    // [has_bias], single-CTA dlogits with kSmallARows-row hidden boxes
   int gh_groups;
   int gw_groups;
 };
@@ -136,7 +154,6 @@ struct FwdParams {
   long long global_V;     // global vocab size (== V unless sharded)
   int f16;                // hidden / weight are IEEE fp16 (else bf16)
   int kps;                // k-blocks per pipeline stage: 2 with 3-D chunked maps (D % 64 == 0), else 1
-  int h_replicas;         // > 1: the hidden map's third dimension selects a copy (single-CTA tiles only)
 };
 
 struct DzParams {
@@ -156,7 +173,6 @@ struct DzParams {
   int* sched_reset;       // [kNumSchedCounters] ticket counters of the gradient GEMMs, zeroed at launch
   int f16;                // hidden / weight / dz are IEEE fp16 (else bf16)
   int kps;                // k-blocks per pipeline stage: 2 with 3-D chunked maps (D % 64 == 0), else 1
-  int h_replicas;         // > 1: the hidden map's third dimension selects a copy (single-CTA tiles only)
 };
 
 // Ticket counters of the in-order scheduled gradient GEMMs (one per GEMM of a
