@@ -3,7 +3,9 @@
 logp / lse rows (and grad_hidden rows) must be bitwise identical whether a
 token is scored alone or inside a batch of 1 / 7 / 64 / 257 / 512 tokens (and
 24 / 25, the last batch whose grad_weight reads copies of the hidden states
-and the first that reads the caller's array), and
+and the first that reads the caller's array; 32 / 33, the last batch whose
+forward and dlogits load 32-row hidden boxes and the first that loads 128),
+and
 every output must be bitwise identical across repeated runs ("Feat/nemotron h
 lm head logprob cuda", Acceptance checks: batch invariance with torch.equal
 across batch sizes and repeat runs)."""
@@ -34,7 +36,7 @@ def pool():
     return inp, d, logp, lse, gh
 
 
-@pytest.mark.parametrize("size", [1, 7, 24, 25, 64, 257])
+@pytest.mark.parametrize("size", [1, 7, 24, 25, 32, 33, 64, 257])
 def test_batch_invariance(pool, size):
     inp, d, logp, lse, gh = pool
     gen = torch.Generator().manual_seed(size)
