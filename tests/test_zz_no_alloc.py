@@ -51,10 +51,12 @@ def _regular(d):
 
 
 CASES = [
-    # (N, D, V, bias, temperature): the Nemotron head near the scratch limit, then a
-    # smaller ragged problem, so the second call runs on the first call's leftovers.
+    # (N, D, V, bias, temperature): the Nemotron head near the scratch limit, then
+    # smaller problems, so each call runs on the previous call's leftovers; the
+    # last one a batch small enough for single-CTA tiles with 32-row hidden boxes.
     (4000, 2688, 131072, False, True),
     (333, 264, 50257, True, False),
+    (20, 2688, 131072, True, True),
 ]
 
 
