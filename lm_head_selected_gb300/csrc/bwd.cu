@@ -235,7 +235,10 @@ struct GradCfg {
   };
 
   static __device__ __forceinline__ uint64_t policy_a() { return l2_policy_evict_normal(); }
-  static __device__ __forceinline__ uint64_t policy_b() { return l2_policy_evict_normal(); }
+  // grad_weight's B, the hidden states, is re-read by every unit
+  static __device__ __forceinline__ uint64_t policy_b() {
+    return (A_MN && LLP_GW_H_EVICT_LAST) ? l2_policy_evict_last() : l2_policy_evict_normal();
+  }
   // units are claimed in ascending order from a ticket counter, so the tiles
   // that share A rows or a K window of B run together
   static constexpr bool DYNAMIC = (LLP_DYNAMIC_SCHED & (A_MN ? 2 : 1)) != 0;

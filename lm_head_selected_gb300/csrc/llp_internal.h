@@ -96,6 +96,10 @@ cudaError_t small_grad_hidden_setup();
 cudaError_t launch_small_grad_hidden(const CUtensorMap& tm_w, const CUtensorMap& tm_dz, const GhSmallParams& p,
                                      int num_sms, cudaStream_t s);
 
+#ifndef LLP_GW_H_EVICT_LAST
+#define LLP_GW_H_EVICT_LAST 1  // grad_weight loads the hidden states with an L2 evict-last hint
+#endif
+
 #ifndef LLP_SMALL_A
 #define LLP_SMALL_A 1        // single-CTA forward / dlogits of <= kSmallARows rows load only those hidden rows
 #endif
