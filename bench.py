@@ -50,7 +50,7 @@ WORKLOADS = {
     "nemotron_n32": (32, 2688, 131072,
                      "Nemotron-3-Nano LM head, N=32 (2x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
                      "uniform targets, grad_logp=1"),
-    # batch 1 x seq 16 on the same head: grad_weight reads per-pair copies of the hidden states
+    # batch 1 x seq 16 on the same head
     "nemotron_n16": (16, 2688, 131072,
                      "Nemotron-3-Nano LM head, N=16 (1x16), D=2688, V=131072, no bias, per-row tau~U[0.7,1.3], "
                      "uniform targets, grad_logp=1"),
@@ -249,8 +249,6 @@ def kernel_model(name, N, D, V, has_bias, has_tau):
         return 0.0, 4.0 * nseg_n * V * D + W
     if name == "bias_sum":
         return 0.0, 4.0 * V * (-(-N // 32)) + 4.0 * V
-    if name == "replicate_hidden":  # one read, eight copies written
-        return 0.0, H + 8.0 * H
     return 0.0, 0.0
 
 

@@ -85,13 +85,7 @@ enum {
  * two-CTA GEMM with the tokens on M.  Both accumulate every element over the
  * same 16-wide vocab slices in the same order, so the results are bitwise the
  * same; LINEAR_LOGP_SMALL_GRAD_HIDDEN=0 before the first call sends small
- * batches through the two-CTA GEMM too (a diagnostic, read once per process).
- *
- * Small-batch note: for a batch of at most 24 rows (and 8 x N x D x 2 bytes of
- * at most 4 MiB, D a multiple of 64) the backward copies the hidden states
- * eight times into its workspace before grad_weight, whose CTA pairs all read
- * the same hidden rows at nearly the same time, and each pair reads one copy.
- * A copy is bit for bit the caller's array, so the results do not change. */
+ * batches through the two-CTA GEMM too (a diagnostic, read once per process). */
 
 /* Bytes of workspace linear_logp_fwd needs for an N x D x V problem
  * (0 when N == 0).  The workspace holds the per-vocab-split (max, sum) pairs
@@ -101,9 +95,8 @@ size_t linear_logp_fwd_workspace_bytes(int64_t N, int64_t D, int64_t V);
 /* Bytes of workspace linear_logp_bwd needs: two work-ticket counters of the
  * gradient GEMMs (set by the library itself; the workspace need not be
  * zeroed), the bf16 dlogits buffer [N, round_up(V, 64)], the grad_bias
- * partials when has_bias != 0, the fp32 K-segment partials of grad_hidden
- * (V > 32768) and grad_weight (N > 32768), and, for a small batch, the copies
- * of the hidden states. */
+ * partials when has_bias != 0, and the fp32 K-segment partials of grad_hidden
+ * (V > 32768) and grad_weight (N > 32768). */
 size_t linear_logp_bwd_workspace_bytes(int64_t N, int64_t D, int64_t V, int has_bias);
 
 /*

@@ -183,9 +183,8 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 }
 
 struct BwdLayout {
-  size_t sched, dz, gb_part, dh_part, dw_part, hrep, total;
+  size_t sched, dz, gb_part, dh_part, dw_part, total;
   bool has_gb, has_dh, has_dw;
-  int h_replicas;  // copies of the hidden states at hrep for grad_weight (1: none)
 };
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, bool want_dw) {
@@ -195,8 +194,6 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool bias, bool want_dh, b
   const size_t nseg_n = static_cast<size_t>(cdiv(N, llp::kKSegment));
   Carver c;
   BwdLayout L;
-  L.h_replicas = want_dw ? llp::hidden_replicas(N, D) : 1;
-  L.hrep = L.h_replicas > 1 ? c.take(static_cast<size_t>(L.h_replicas) * N * D * 2) : 0;
   L.sched = c.take(llp::kNumSchedCounters * sizeof(int));
   L.dz = c.take(static_cast<size_t>(N) * V_pad * 2);
   L.has_gb = bias;
@@ -276,14 +273,12 @@ enum KernelId {
   kKSegSumHidden,
   kKSegSumWeight,
   kKBiasSum,
-  kKReplicateHidden,
   kKNumKernels
 };
 
 const char* const kKernelNames[kKNumKernels] = {"fwd_partials",  "fwd_merge",          "dlogits",
                                                 "grad_hidden",   "grad_weight",        "segment_sum_hidden",
-                                                "segment_sum_weight", "bias_sum",
-                                                "replicate_hidden"};
+                                                "segment_sum_weight", "bias_sum"};
 
 struct Recorder {
   std::mutex mu;
@@ -333,22 +328,6 @@ RowTiling row_tiling(int64_t N) {
 // would leave only one in flight while the MMAs read the other, and with
 // 32-row boxes three double stages ran no faster than six single ones.
 int k_blocks_per_stage(int64_t D, bool single) { return ((LLP_KPS2 & 1) && !single && (D % 64) == 0) ? 2 : 1; }
-
-// 4-D form of make_map_chunked over R copies laid end to end:
-// {64, rows, cols / 64, R}, a box taking one copy.
-int make_map_chunked_replicas(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, int R,
-                              uint32_t box_rows, uint32_t box_chunks, bool f16) {
-  cuuint64_t dims[4] = {64, rows, cols / 64, static_cast<cuuint64_t>(R)};
-  cuuint64_t strides[3] = {cols * 2, 128, cols * rows * 2};
-  cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) g_last_driver_result = static_cast<int>(r);
-  return r == CUDA_SUCCESS ? LLP_OK : fail_cuda(__LINE__);
-}
 
 // Tensor maps of the two K-major operands of the forward / dlogits GEMMs, the
 // hidden states (box rows kTileM) and the weight (box rows w_box_rows): 2-D with
@@ -549,7 +528,6 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
       p.a_chunked = 0;
       p.b_chunked = w_chunked ? 1 : 0;
       p.kps = kps;
-      p.h_replicas = 1;
       p.rows = static_cast<int>(N);
       p.D = static_cast<int>(D);
       p.K = static_cast<int>(V);
@@ -599,18 +577,7 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     } else if (make_map(&tm_dz_mn, dz, V, N, V_pad * 2, 64, llp::kTileK, f16) != LLP_OK) {
       return fail_cuda(__LINE__);
     }
-    // copies of a small batch's hidden states: every CTA pair reads all of
-    // them at nearly the same k-block, and one copy sits in a few L2 slices
-    const int gw_reps = L.h_replicas > 1 && h_chunked && kps == 1 ? L.h_replicas : 1;
-    if (gw_reps > 1) {
-      if (llp::launch_replicate(hidden, static_cast<size_t>(N) * D * 2, gw_reps, ws + L.hrep, dev->num_sms, s) !=
-          cudaSuccess)
-        return fail_cuda(__LINE__);
-      rec_mark(s, kKReplicateHidden);
-      if (make_map_chunked_replicas(&tm_h_mn, ws + L.hrep, D, N, gw_reps, llp::kTileK, llp::kBRows / 64, f16) !=
-          LLP_OK)
-        return fail_cuda(__LINE__);
-    } else if (h_chunked) {
+    if (h_chunked) {
       if (make_map_chunked(&tm_h_mn, hidden, D, N, D * 2, llp::kTileK * kps, llp::kBRows / 64, f16) != LLP_OK)
         return fail_cuda(__LINE__);
     } else if (make_map(&tm_h_mn, hidden, D, N, D * 2, 64, llp::kTileK, f16) != LLP_OK) {
@@ -620,7 +587,6 @@ int bwd_core(DeviceInit* dev, const float* grad_logp, const float* saved_lse, co
     p.a_chunked = dz_chunked ? 1 : 0;
     p.b_chunked = h_chunked ? 1 : 0;
     p.kps = kps;
-    p.h_replicas = gw_reps;
     p.rows = static_cast<int>(V);
     p.D = static_cast<int>(D);
     p.K = static_cast<int>(N);

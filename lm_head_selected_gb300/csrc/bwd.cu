@@ -95,7 +95,6 @@ struct DzCfg {
   static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
   static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
   static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
-  static __device__ __forceinline__ int b_replicas(const Params&) { return 1; }
   // the gradient GEMMs that follow on the stream start from ticket 0
   static __device__ __forceinline__ void on_launch(const Params& p) {
     if (p.sched_reset != nullptr)
@@ -248,7 +247,6 @@ struct GradCfg {
   static __device__ __forceinline__ bool b_chunked(const Params& p) { return p.b_chunked != 0; }
   static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
   // grad_weight's B is the hidden states
-  static __device__ __forceinline__ int b_replicas(const Params& p) { return A_MN ? p.h_replicas : 1; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.nseg * p.num_m * p.num_d; }
@@ -360,15 +358,6 @@ __global__ void __launch_bounds__(256) segment_sum_f32_kernel(const float* __res
   }
 }
 
-// dst[r][i] = src[i] for r < R: R copies of a small buffer, 16 bytes per thread step.
-__global__ void __launch_bounds__(256) replicate_kernel(const uint4* __restrict__ src, long long n16, int R,
-                                                        uint4* __restrict__ dst) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
-    const uint4 v = src[i];
-    for (int r = 0; r < R; ++r) dst[static_cast<size_t>(r) * n16 + i] = v;
-  }
-}
-
 // grad_bias[v] = sum over 32-row blocks in ascending order.
 __global__ void __launch_bounds__(256) bias_sum_kernel(const float* __restrict__ gb_part, int nblocks, int V,
                                                        float* __restrict__ out) {
@@ -442,18 +431,6 @@ cudaError_t launch_segment_sum_f32(const float* part, int nseg, long long count,
   const int threads = 256;
   const long long blocks = segment_sum_blocks(count, threads, num_sms);
   segment_sum_f32_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(part, nseg, count, out);
-  return launch_result();
-}
-
-cudaError_t launch_replicate(const void* src, size_t bytes, int R, void* dst, int num_sms, cudaStream_t s) {
-  const long long n16 = static_cast<long long>(bytes / 16);
-  const int threads = 256;
-  long long blocks = (n16 + threads - 1) / threads;
-  const long long cap = 4LL * (num_sms > 0 ? num_sms : 1);
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  replicate_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(static_cast<const uint4*>(src), n16, R,
-                                                                static_cast<uint4*>(dst));
   return launch_result();
 }
 

@@ -61,7 +61,6 @@ struct FwdCfg {
   static __device__ __forceinline__ bool a_chunked(const Params&) { return false; }
   static __device__ __forceinline__ bool b_chunked(const Params&) { return false; }
   static __device__ __forceinline__ int kps(const Params& p) { return p.kps; }
-  static __device__ __forceinline__ int b_replicas(const Params&) { return 1; }
   static __device__ __forceinline__ void on_launch(const Params&) {}
 
   static __device__ __forceinline__ int num_units(const Params& p) { return p.num_m * p.num_splits; }

@@ -260,10 +260,6 @@ __device__ __forceinline__ void run_producer_k(const SharedState& st, const CUte
   // decides anything about the arithmetic.
   unsigned int* const prog = dyn && leader ? Cfg::progress_counter(p) : nullptr;
   const unsigned int npairs = gridDim.x / P::NCTA;
-  // Copies of an operand that every CTA pair re-reads (grad_weight's hidden
-  // states of a small batch): each pair reads its own, so the few L2 slices
-  // that would hold a single copy do not serve the whole launch.
-  const int b_reps = Cfg::b_replicas(p);
   unsigned int mine = 0;
   for (int k = 0;; ++k) {
     int u;
@@ -326,10 +322,7 @@ __device__ __forceinline__ void run_producer_k(const SharedState& st, const CUte
             else
               tma_load_2d_pair(sB, tmB, bar, kx, b_row, polB);
           } else if (Cfg::b_chunked(p)) {
-            if (b_reps > 1)  // this pair's copy of a small, hot operand
-              tma_load_4d_pair(sB, tmB, bar, 0, kx, b_row / 64, static_cast<int>(blockIdx.x / P::NCTA) % b_reps, polB);
-            else
-              tma_load_3d_pair(sB, tmB, bar, 0, kx, b_row / 64, polB);
+            tma_load_3d_pair(sB, tmB, bar, 0, kx, b_row / 64, polB);
           } else {
             for (int i = 0; i < b_rows / 64; ++i) tma_load_2d_pair(sB + i * 8192, tmB, bar, b_row + 64 * i, kx, polB);
           }
@@ -353,10 +346,7 @@ __device__ __forceinline__ void run_producer_k(const SharedState& st, const CUte
             else
               tma_load_2d(sB, tmB, &st.full[stage], kx, b_row, polB);
           } else if (Cfg::b_chunked(p)) {
-            if (b_reps > 1)
-              tma_load_4d(sB, tmB, &st.full[stage], 0, kx, b_row / 64, static_cast<int>(blockIdx.x) % b_reps, polB);
-            else
-              tma_load_3d(sB, tmB, &st.full[stage], 0, kx, b_row / 64, polB);
+            tma_load_3d(sB, tmB, &st.full[stage], 0, kx, b_row / 64, polB);
           } else {
             for (int i = 0; i < b_rows / 64; ++i)
               tma_load_2d(sB + i * 8192, tmB, &st.full[stage], b_row + 64 * i, kx, polB);

@@ -98,6 +98,7 @@ cudaError_t launch_small_grad_hidden(const CUtensorMap& tm_w, const CUtensorMap&
 
 #ifndef LLP_GW_H_EVICT_LAST
 #define LLP_GW_H_EVICT_LAST 1  // grad_weight loads the hidden states with an L2 evict-last hint
+                               // (every unit re-reads them; at small N all pairs read the same few lines)
 #endif
 
 #ifndef LLP_SMALL_A
@@ -115,20 +116,6 @@ constexpr int kSmallADzStages = 5;   // 5 x 36 KB + the epilogue's 32 KB of stor
 inline int hidden_box_rows(long long N, bool single) {
   return (LLP_SMALL_A && single && N <= kSmallARows) ? kSmallARows : kTileM;
 }
-
-#ifndef LLP_H_REPLICA_MAX_N
-#define LLP_H_REPLICA_MAX_N 24   // batches of at most this many rows give grad_weight per-pair hidden-state copies (0: off)
-#endif
-// Copies of a small batch's hidden states for grad_weight: every CTA pair
-// re-reads all of them at nearly the same k-block, and a single copy sits in a
-// few L2 slices that then serve the whole launch.
-constexpr int kHReplicas = 8;
-constexpr long long kHReplicaMaxBytes = 4ll << 20;  // all copies together
-inline int hidden_replicas(long long N, long long D) {
-  return (N <= LLP_H_REPLICA_MAX_N && kHReplicas * N * D * 2 <= kHReplicaMaxBytes) ? kHReplicas : 1;
-}
-// dst = R consecutive copies of the `bytes` bytes at src (16-byte multiples, 16-byte aligned).
-cudaError_t launch_replicate(const void* src, size_t bytes, int R, void* dst, int num_sms, cudaStream_t s);
 
 // Resident work groups (CTA pairs, or CTAs in single mode) per GEMM kernel,
 // found once per device; the persistent grids never exceed them.
@@ -197,7 +184,6 @@ struct GradGemmParams {
   unsigned int* progress;  // k-blocks issued by all pairs, 0 at launch (advisory lockstep); nullptr: off
   int a_chunked, b_chunked;  // the MN-major operand's map is 3-D {64, K, MN/64}: one copy per stage
   int kps;             // k-blocks per pipeline stage: 2 when every operand map is 3-D, else 1
-  int h_replicas;      // grad_weight: > 1, the chunked hidden map's fourth dimension selects a copy
   int f16;             // operands and the 16-bit output are IEEE fp16 (else bf16)
 };
 

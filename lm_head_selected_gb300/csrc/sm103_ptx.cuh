@@ -171,16 +171,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const CUtensorMap
       : "memory");
 }
 
-// 4-D form: coordinates {x, y, z, w}, x innermost.
-__device__ __forceinline__ void tma_load_4d(uint32_t smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                            int z, int w, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // TMA stores (shared -> global), tracked per thread with bulk groups.  The
 // tensor map clips rows / columns outside the tensor, so partial tiles are safe.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -387,16 +377,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t smem_dst, const CUtens
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr), "l"(policy)
-      : "memory");
-}
-
-// 4-D form of tma_load_2d_pair: coordinates {x, y, z, w}, x innermost.
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t smem_dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
-                                                 int x, int y, int z, int w, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster_addr), "l"(policy)
       : "memory");
 }
 

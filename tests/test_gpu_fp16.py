@@ -26,7 +26,7 @@ SHAPES = [
     (257, 512, 2048, False, True),     # three M tiles, the last with one row
     (96, 2688, 4096, True, False),     # full Nemotron hidden size
     (64, 128, 32832, False, False),    # two vocab K segments of grad_hidden
-    (20, 256, 5000, True, True),       # small batch: 32-row hidden boxes, grad_weight on hidden-state copies
+    (20, 256, 5000, True, True),       # small batch: single-CTA tiles with 32-row hidden boxes
 ]
 
 

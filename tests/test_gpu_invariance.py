@@ -2,10 +2,8 @@
 
 logp / lse rows (and grad_hidden rows) must be bitwise identical whether a
 token is scored alone or inside a batch of 1 / 7 / 64 / 257 / 512 tokens (and
-24 / 25, the last batch whose grad_weight reads copies of the hidden states
-and the first that reads the caller's array; 32 / 33, the last batch whose
-forward and dlogits load 32-row hidden boxes and the first that loads 128),
-and
+32 / 33, the last batch whose forward and dlogits load 32-row hidden boxes and
+the first that loads 128-row ones), and
 every output must be bitwise identical across repeated runs ("Feat/nemotron h
 lm head logprob cuda", Acceptance checks: batch invariance with torch.equal
 across batch sizes and repeat runs)."""

@@ -53,7 +53,7 @@ SHAPES = [
     (40, 64, 200000, True, False, 2, 1),  # 391 vocab splits, ragged last split
     # >= 1024 tokens: grad_weight takes two k-blocks per stage; D = 3 x 64 is an odd number of 64-column
     # chunks, so a copy's second chunk of hidden runs past D (read as zeros)
-    (16, 2688, 33000, True, True, 2, 1),  # small batch: grad_weight reads per-pair copies of the hidden states
+    (16, 2688, 33000, True, True, 2, 1),  # small batch: single-CTA tiles with 32-row hidden boxes
     (1100, 192, 3000, True, True, 3, 1),
     (1030, 200, 2500, False, True, 2, 0),  # D not a multiple of 64: every GEMM on one k-block per stage, 2-D maps
 ]
