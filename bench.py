@@ -76,11 +76,11 @@ PAGES_CONTEXT = "H100 PCIe, strict cuBLASLt fwd+bwd 351.2 ms at 16384 tokens (co
 # valid only while the kernel sources are unchanged (checked by sources_sha).
 NCU_TRAFFIC = {
     "workload": "rl_head_fwd_bwd",
-    "sources_sha": "7b6cd6aa3e060d57",
+    "sources_sha": "78e648d649a7c836",
     "how": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch per kernel (ncu -k one kernel, -c 1, "
             "1 pass), full-size workload, one box; box-to-box spread for the same build is large"),
-    "bytes_per_launch": {"fwd_partials": 1545288000 + 36868864, "dlogits": 2514025000 + 4270045000,
-                         "grad_hidden": 15080903000 + 698669824, "grad_weight": 11418353000 + 700805888},
+    "bytes_per_launch": {"fwd_partials": 4217778000 + 36973056, "dlogits": 6445659000 + 4277988000,
+                         "grad_hidden": 26158636000 + 696774400, "grad_weight": 11885443000 + 705190400},
 }
 
 GEMM_KERNELS = ("fwd_partials", "dlogits", "grad_hidden", "grad_weight")
